@@ -1,0 +1,398 @@
+"""Throughput of the attention forward pass on GB300, one JSON line.
+
+A step is one forward pass (one kernel launch) over one batch of seeded
+synthetic inputs already resident in HBM.  The default workload is causal GQA
+attention, B=2, Hq=32, Hkv=8, Sq=Skv=4096, D=128, bf16 -- the configuration
+the headline metric (attention forward TFLOP/s, bf16 causal, S=4096, D=128)
+is quoted on.  FLOPs per step = 4*B*Hq*Sq*Skv*D, halved for causal.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, same metric
+
+For N > 1 (torchrun, one rank per GPU) every rank runs its own replica of the
+workload (weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (bf16 causal, S=4096, D=128) and % of GB300 tensor peak"
+L2_BYTES = 129 * 1024 * 1024
+
+# name -> (B, Hq, Hkv, S, D, causal, dtype)
+WORKLOADS = {
+    "gqa-causal-4096": (2, 32, 8, 4096, 128, True, "bf16"),
+    "tiny-mha": (1, 2, 2, 128, 64, False, "bf16"),
+    "mha-causal-1024": (4, 16, 16, 1024, 64, True, "bf16"),
+    "fp8-causal-8192": (2, 16, 16, 8192, 128, True, "e4m3"),
+}
+for _B, _S in [(64, 512), (32, 1024), (16, 2048), (8, 4096), (4, 8192), (2, 16384)]:
+    WORKLOADS[f"mqa-causal-{_S}"] = (_B, 32, 1, _S, 128, True, "bf16")
+    WORKLOADS[f"mqa-full-{_S}"] = (_B, 32, 1, _S, 128, False, "bf16")
+DEFAULT_WORKLOAD = "gqa-causal-4096"
+
+
+def describe(name):
+    B, Hq, Hkv, S, D, causal, dtype = WORKLOADS[name]
+    return f"{'causal' if causal else 'non-causal'} B={B} Hq={Hq} Hkv={Hkv} Sq=Skv={S} D={D} {dtype}"
+
+
+def step_flops(name):
+    B, Hq, Hkv, S, D, causal, _ = WORKLOADS[name]
+    f = 4.0 * B * Hq * S * S * D
+    return f / 2 if causal else f
+
+
+def step_bytes(name):
+    """Algorithmic bytes: Q, K, V read once and O written once."""
+    B, Hq, Hkv, S, D, _, dtype = WORKLOADS[name]
+    e_in = 1 if dtype == "e4m3" else 2
+    return B * S * D * (Hq * e_in + 2 * Hkv * e_in + Hq * 2)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "scaled_dot_product_05_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def stored_traffic(name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources and this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    e = t.get(name)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, timestamped."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not inside:
+            # region shorter than the sampling period: nearest samples under load
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            inside = [p for _, p in near]
+            note = "timed region shorter than the 50 ms sampling period; nearest samples"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+# --------------------------------------------------------------- CPU leg ----
+
+def oracle_sample(name, seconds_target=12.0, threads=0):
+    """Time the fp64 oracle on a seeded sample of output rows of the workload;
+    returns (TFLOP/s, cores, description)."""
+    import numpy as np
+    import oracle
+    from sdpa_inputs import make_qkv
+
+    B, Hq, Hkv, S, D, causal, dtype = WORKLOADS[name]
+    x = make_qkv(1000, B, Hq, Hkv, S, S, D, dtype)
+    rng = np.random.default_rng(1001)
+    total_rows = B * S * Hq
+
+    def flops_of(rows):
+        i = (np.asarray(rows) // Hq) % S
+        vis = np.minimum(i + 1, S) if causal else np.full(len(rows), S)
+        return 4.0 * D * float(vis.sum())
+
+    def run(rows):
+        t0 = time.perf_counter()
+        oracle.sdpa_reference(x.q, x.k, x.v, causal=causal, dtype=dtype, descales=x.descales, rows=rows,
+                              threads=threads)
+        return time.perf_counter() - t0
+
+    n = 256
+    rows = np.sort(rng.choice(total_rows, size=min(n, total_rows), replace=False))
+    dt = run(rows)
+    rate = flops_of(rows) / max(dt, 1e-9)
+    # size the timed sample to about `seconds_target` seconds of CPU work
+    mean_row = flops_of(rows) / len(rows)
+    n = int(min(total_rows, max(64, seconds_target * rate / mean_row)))
+    rows = np.sort(rng.choice(total_rows, size=n, replace=False))
+    dt = run(rows)
+    f = flops_of(rows)
+    return f / dt / 1e12, oracle.last_threads(), (
+        f"{n} of {total_rows} output rows of the workload, uniformly sampled (seed 1001), "
+        f"{f / 1e9:.1f} GFLOP in {dt:.1f} s")
+
+
+def run_reference(args, rank, world):
+    name = args.workload
+    if rank != 0:
+        return 0
+    import numpy as np  # noqa: F401
+    B, Hq, Hkv, S, D, causal, dtype = WORKLOADS[name]
+    per_step_target = max(1.0, min(20.0, 90.0 / max(1, args.steps + args.warmup)))
+    values = []
+    desc, cores = "", 0
+    for i in range(args.warmup + args.steps):
+        tf, cores, desc = oracle_sample(name, seconds_target=per_step_target)
+        if i >= args.warmup:
+            values.append(tf)
+    value = statistics.median(values)
+    ms = step_flops(name) / (value * 1e12) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": describe(name), "flops_per_step": step_flops(name),
+                   "note": "fp64 CPU oracle on the host cores; each step times a bounded row sample and "
+                           "ms_per_step is extrapolated to the whole workload"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- GPU leg ----
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from scaled_dot_product_05_gb300 import sdpa_device_error, sdpa_fwd, sdpa_fwd_fp8
+    from sdpa_inputs import make_qkv
+
+    name = args.workload
+    B, Hq, Hkv, S, D, causal, dtype = WORKLOADS[name]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    # two resident input sets (different seeds) used alternately, so a step
+    # never finds its inputs in L2 from the previous step
+    sets = []
+    host = None
+    for s in range(2):
+        x = make_qkv(100 + 17 * rank + s, B, Hq, Hkv, S, S, D, dtype)
+        q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+        o = torch.empty((B, S, Hq, D), dtype=torch.bfloat16 if dtype == "e4m3" else q.dtype, device=dev)
+        sets.append((q, k, v, o, x.descales))
+        if s == 0:
+            host = x
+
+    def launch(i, tensors=None):
+        q, k, v, o, ds = tensors if tensors is not None else sets[i & 1]
+        if dtype == "e4m3":
+            sdpa_fwd_fp8(q, k, v, o, descale_q=ds[0], descale_k=ds[1], descale_v=ds[2], causal=causal,
+                         stream=stream)
+        else:
+            sdpa_fwd(q, k, v, o, causal=causal, stream=stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        launch(i)
+    barrier()
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        launch(i)
+        ev[i][1].record(stream)
+    end.record(stream)
+    barrier()
+    t_wall1 = time.time()
+    total_ms = start.elapsed_time(end)
+    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    err = sdpa_device_error()
+    if err:
+        raise RuntimeError(f"device error word 0x{err:x}")
+
+    # ---- end to end: pinned host inputs -> device -> kernel -> host output --
+    e2e_steps = max(3, min(args.steps, 20))
+    hq_, hk_, hv_ = (t.pin_memory() for t in (host.q, host.k, host.v))
+    q, k, v, o, ds = sets[0]
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    bi = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_))
+    bo = ho.numel() * ho.element_size()
+
+    def e2e_step():
+        q.copy_(hq_, non_blocking=True)
+        k.copy_(hk_, non_blocking=True)
+        v.copy_(hv_, non_blocking=True)
+        launch(0, (q, k, v, o, ds))
+        ho.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if sampler:
+        sampler.stop()
+
+    if rank != 0:
+        return 0
+
+    flops = step_flops(name)
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    avg_kernel_ms = statistics.mean(kern_ms)
+    achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
+    if dtype == "e4m3":
+        peak = peaks["bf16_tflops"] * 2.0       # FP8 dense rate is twice bf16's (4.5 vs 2.25 PF nominal)
+        peak_note = f"bf16 burst ({peak_src}) x 2 nominal FP8/bf16 ratio"
+    else:
+        peak = peaks["bf16_tflops"]
+        peak_note = f"bf16 burst ({peak_src})"
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": stored_traffic(name),
+                "peak_source": peak_note, "kernel": "sdpa_fwd_kernel",
+                "algorithmic_bytes_per_launch": step_bytes(name),
+                "achieved_hbm_gbs": step_bytes(name) / (avg_kernel_ms * 1e-3) / 1e9,
+                "hbm_peak_gbs": peaks["hbm_gbs"]}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded N(0,1), inputs resident in HBM)",
+        "config": {"workload": describe(name), "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": S, "Skv": S, "D": D,
+                   "causal": causal, "flops_per_step": flops, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 ({step_bytes(name) / 1e6:.1f} MB per step, 2 rotating sets)"},
+        "roofline": roofline,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
+    }
+    if not args.no_cpu_baseline:
+        tf, cores, desc = oracle_sample(name, seconds_target=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        return run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

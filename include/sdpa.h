@@ -1,0 +1,125 @@
+/*
+ * sdpa.h -- C ABI of the GB300 (sm_103a) scaled dot-product attention
+ * forward pass.
+ *
+ * Operation.  Codelab "Attention on GPU (cuDNN and TransformerEngine)",
+ * section 1 ("How attention works"):
+ *
+ *     O = softmax(Q K^T * scale [+ causal mask]) V
+ *
+ * computed per (batch, query head) in one fused kernel that never writes the
+ * Sq x Skv weight matrix to memory (section 8, "Run benchmarks", sequence
+ * sweep: fused kernels tile the computation instead of materialising it).
+ *
+ * Layout (section 3, "Create Q, K and V test arrays": (B, T, N, H)), all
+ * contiguous, head dimension innermost:
+ *     Q, O : [B][Sq][Hq][D]
+ *     K, V : [B][Skv][Hkv][D]
+ * Heads (section 9, "Compare MHA, GQA and MQA"): Hkv divides Hq and query
+ * head hq reads KV head hq / (Hq / Hkv) -- MHA (Hkv = Hq), GQA, MQA (Hkv = 1).
+ * Causal (section 7, "Add causal masking"): the lower triangle of the
+ * Sq x Skv score matrix is kept, i.e. query row i sees keys 0..i (top-left
+ * aligned when Sq != Skv; rows i >= Skv see every key).
+ *
+ * Ownership and execution.  The caller owns every buffer; all of Q, K, V and
+ * O are device pointers (cudaMalloc / PyTorch CUDA tensors) except where a
+ * function says otherwise.  The library allocates no device memory.  Work is
+ * enqueued on `stream` (a cudaStream_t; NULL means the legacy default stream)
+ * and the call returns without synchronising.
+ *
+ * Errors.  Every argument is checked before any CUDA call; on a failed check
+ * the function returns a status code, enqueues nothing and leaves O
+ * untouched.  There is no fallback to another implementation (section 6,
+ * "Force the cuDNN fused backend": an unsupported request is an error, not a
+ * silent switch).  A launch failure returns SDPA_ERR_CUDA; the CUDA error is
+ * available from sdpa_last_cuda_error().  A kernel that had to give up (a
+ * bounded wait inside it expired) records a code in a device error word that
+ * sdpa_device_error() reads.
+ */
+#ifndef SDPA_GB300_H
+#define SDPA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SDPA_DTYPE_BF16 = 0,   /* bfloat16 Q, K, V and O */
+    SDPA_DTYPE_FP16 = 1,   /* IEEE binary16 Q, K, V and O */
+    SDPA_DTYPE_E4M3 = 2    /* FP8 E4M3 Q, K, V; bfloat16 O (sdpa_fwd_fp8 only) */
+} sdpa_dtype_t;
+
+typedef enum {
+    SDPA_OK = 0,
+    SDPA_ERR_NULL_PTR = 1,     /* a required pointer is NULL */
+    SDPA_ERR_MISALIGNED = 2,   /* a pointer is not 16-byte aligned */
+    SDPA_ERR_BAD_SHAPE = 3,    /* a size is < 1 or too large */
+    SDPA_ERR_HEADS = 4,        /* Hq is not a multiple of Hkv */
+    SDPA_ERR_HEAD_DIM = 5,     /* D is not 64 or 128 */
+    SDPA_ERR_DTYPE = 6,        /* unknown dtype, or E4M3 passed to sdpa_fwd */
+    SDPA_ERR_SCALE = 7,        /* scale (or a descale) is not finite and > 0 */
+    SDPA_ERR_ARCH = 8,         /* current device is not compute capability 10.3 */
+    SDPA_ERR_ALIAS = 9,        /* O overlaps Q, K or V */
+    SDPA_ERR_CUDA = 10         /* a CUDA call failed; see sdpa_last_cuda_error() */
+} sdpa_status_t;
+
+/*
+ * Attention forward pass, bf16 or fp16 (section 6: the fused backend takes
+ * 16-bit inputs).
+ *   Q, K, V   device, read only, layout above, element type `dtype`.
+ *   O         device, written, [B][Sq][Hq][D], element type `dtype`; must not
+ *             overlap Q, K or V.
+ *   B, Hq, Hkv, Sq, Skv   >= 1, Hq % Hkv == 0.
+ *   D         64 or 128.
+ *   scale     finite, > 0; section 4 ("Implement attention from scratch")
+ *             uses 1/sqrt(D).
+ *   causal    0 = no mask, nonzero = lower-triangular mask.
+ *   dtype     SDPA_DTYPE_BF16 or SDPA_DTYPE_FP16.
+ *   stream    cudaStream_t to enqueue on.
+ * All pointers must be 16-byte aligned.  Scores and the softmax statistics
+ * are fp32; O is rounded to nearest even.
+ */
+sdpa_status_t sdpa_fwd(const void *Q, const void *K, const void *V, void *O,
+                       int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                       float scale, int causal, sdpa_dtype_t dtype, void *stream);
+
+/*
+ * FP8 forward pass (section 10, "Benchmark NVIDIA TransformerEngine and FP8":
+ * E4M3 for the forward pass, per-tensor scales from the absolute maximum).
+ *   Q, K, V   device, E4M3 bytes; the real value of an element is
+ *             code * descale_x (descale_x = amax(x) / 448 for a tensor
+ *             quantised with scale 448 / amax(x)).
+ *   O         device, bfloat16, [B][Sq][Hq][D].
+ *   descale_q, descale_k, descale_v   finite, > 0.
+ * The softmax weights P are quantised to E4M3 (times 448) before P V, with an
+ * fp32 accumulator; other arguments as for sdpa_fwd.
+ */
+sdpa_status_t sdpa_fwd_fp8(const void *Q, const void *K, const void *V, void *O,
+                           int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                           float scale, float descale_q, float descale_k, float descale_v,
+                           int causal, void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *sdpa_status_string(sdpa_status_t status);
+
+/* cudaError_t (as int) of the most recent SDPA_ERR_CUDA on this thread. */
+int sdpa_last_cuda_error(void);
+
+/*
+ * Reads and clears the device error word of the current device (0 = none;
+ * 0x1xx / 0x2xx / 0x3xx = a bounded wait of the producer / MMA issuer /
+ * softmax gave up).  Synchronises the device.  Returns SDPA_OK or
+ * SDPA_ERR_CUDA; `code` (host pointer) receives the word.
+ */
+sdpa_status_t sdpa_device_error(unsigned int *code);
+
+/* Version of this ABI (bumped on any incompatible change). */
+int sdpa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_GB300_H */

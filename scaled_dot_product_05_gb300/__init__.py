@@ -1,0 +1,91 @@
+"""GB300 (sm_103a) scaled dot-product attention forward pass.
+
+Python binding of the C ABI in include/sdpa.h.  Every step of the computation
+runs in the CUDA library; these functions only marshal PyTorch CUDA tensors
+(used for device memory and streams) into the C call.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _abi
+from ._abi import SdpaError, check, lib, status_string
+
+__all__ = ["sdpa_fwd", "sdpa_fwd_fp8", "sdpa_status_string", "sdpa_device_error", "SdpaError", "lib"]
+
+_DTYPE = {torch.bfloat16: _abi.SDPA_DTYPE_BF16, torch.float16: _abi.SDPA_DTYPE_FP16}
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _shapes(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("Q, K, V must be [B, S, H, D]")
+    B, Sq, Hq, D = q.shape
+    _, Skv, Hkv, _ = k.shape
+    return B, Hq, Hkv, Sq, Skv, D
+
+
+def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor | None = None, *,
+             causal: bool = False, scale: float | None = None, stream=None) -> torch.Tensor:
+    """O = softmax(Q K^T * scale [+ causal mask]) V on the GPU.
+
+    q: [B, Sq, Hq, D], k and v: [B, Skv, Hkv, D], bf16 or fp16 contiguous CUDA
+    tensors (shape agreement is checked by the library).  Returns ``o``
+    (allocated like ``q`` when not given)."""
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if k.shape != v.shape or k.shape[0] != q.shape[0] or k.shape[3] != q.shape[3] or q.dtype != k.dtype \
+            or q.dtype != v.dtype:
+        raise ValueError("K and V must be [B, Skv, Hkv, D] like Q, with Q's dtype")
+    B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+    if o is None:
+        o = torch.empty_like(q)
+    elif not o.is_cuda or not o.is_contiguous() or o.shape != q.shape or o.dtype != q.dtype:
+        raise ValueError("o must be a contiguous CUDA tensor shaped and typed like q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dt = _DTYPE.get(q.dtype, 99)
+    check(lib().sdpa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
+                         float(scale), int(bool(causal)), dt, _stream_ptr(stream)))
+    return o
+
+
+def sdpa_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor | None = None, *,
+                 descale_q: float, descale_k: float, descale_v: float, causal: bool = False,
+                 scale: float | None = None, stream=None) -> torch.Tensor:
+    """FP8 E4M3 inputs (``torch.float8_e4m3fn`` or uint8 codes) with
+    per-tensor descales; bf16 output."""
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.element_size() != 1:
+            raise ValueError("inputs must be contiguous 1-byte CUDA tensors")
+    B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+    if o is None:
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    elif not o.is_cuda or not o.is_contiguous() or o.shape != q.shape or o.dtype != torch.bfloat16:
+        raise ValueError("o must be a contiguous bf16 CUDA tensor shaped like q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    check(lib().sdpa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
+                             float(scale), float(descale_q), float(descale_k), float(descale_v),
+                             int(bool(causal)), _stream_ptr(stream)))
+    return o
+
+
+def sdpa_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def sdpa_device_error() -> int:
+    """Read and clear the device error word (synchronises the device)."""
+    code = ctypes.c_uint(0)
+    check(lib().sdpa_device_error(ctypes.byref(code)))
+    return int(code.value)

@@ -1,0 +1,67 @@
+"""ctypes view of the C ABI in include/sdpa.h (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH
+
+SDPA_DTYPE_BF16, SDPA_DTYPE_FP16, SDPA_DTYPE_E4M3 = 0, 1, 2
+STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_NULL_PTR", 2: "SDPA_ERR_MISALIGNED", 3: "SDPA_ERR_BAD_SHAPE",
+          4: "SDPA_ERR_HEADS", 5: "SDPA_ERR_HEAD_DIM", 6: "SDPA_ERR_DTYPE", 7: "SDPA_ERR_SCALE",
+          8: "SDPA_ERR_ARCH", 9: "SDPA_ERR_ALIAS", 10: "SDPA_ERR_CUDA"}
+# every function include/sdpa.h declares
+EXPORTS = ("sdpa_fwd", "sdpa_fwd_fp8", "sdpa_status_string", "sdpa_last_cuda_error",
+           "sdpa_device_error", "sdpa_abi_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SdpaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def _bind(lib):
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.sdpa_fwd.restype = i
+    lib.sdpa_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+    lib.sdpa_fwd_fp8.restype = i
+    lib.sdpa_fwd_fp8.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, f, f, f, i, vp]
+    lib.sdpa_status_string.restype = ctypes.c_char_p
+    lib.sdpa_status_string.argtypes = [i]
+    lib.sdpa_last_cuda_error.restype = i
+    lib.sdpa_last_cuda_error.argtypes = []
+    lib.sdpa_device_error.restype = i
+    lib.sdpa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    lib.sdpa_abi_version.restype = i
+    lib.sdpa_abi_version.argtypes = []
+    return lib
+
+
+def lib():
+    """The loaded CUDA library.  Raises if it has not been built: there is no
+    other implementation to fall back to."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"CUDA library not built ({LIB_PATH}); run "
+                                  "`python -c 'import __graft_entry__ as g; g.build()'`")
+            _lib = _bind(ctypes.CDLL(LIB_PATH))
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().sdpa_status_string(int(status)).decode()
+
+
+def check(status: int) -> None:
+    if status != 0:
+        msg = status_string(status)
+        if status == 10:
+            msg += f" (cudaError {lib().sdpa_last_cuda_error()})"
+        raise SdpaError(status, msg)

@@ -1,0 +1,95 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+function include/sdpa.h declares, and rejects bad arguments with the
+documented status before any CUDA call."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+import torch
+
+from scaled_dot_product_05_gb300 import _abi
+from scaled_dot_product_05_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return _abi.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(sdpa_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert names, "no declarations found"
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared but not exported"
+    assert set(names) == set(_abi.EXPORTS)
+
+
+def test_abi_version_and_strings(lib):
+    assert lib.sdpa_abi_version() >= 1
+    for code in range(11):
+        s = lib.sdpa_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.sdpa_status_string(99).decode() == "unknown status"
+
+
+# fake, never dereferenced, 16-byte aligned device addresses, far apart
+QP, KP, VP, OP = 0x10000000, 0x20000000, 0x30000000, 0x40000000
+GOOD = dict(B=2, Hq=8, Hkv=2, Sq=300, Skv=300, D=128, scale=1 / math.sqrt(128), causal=1, dtype=0)
+
+
+def call(lib, q=QP, k=KP, v=VP, o=OP, **kw):
+    a = dict(GOOD, **kw)
+    return lib.sdpa_fwd(q, k, v, o, a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Skv"], a["D"],
+                        ctypes.c_float(a["scale"]), a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1),
+    (dict(q=QP + 8), 2), (dict(o=OP + 2), 2),
+    (dict(B=0), 3), (dict(Hq=0), 3), (dict(Hkv=0), 3), (dict(Sq=0), 3), (dict(Skv=0), 3), (dict(Sq=-5), 3),
+    (dict(B=1 << 20, Hq=1 << 12), 3),
+    (dict(Hq=6, Hkv=4), 4),
+    (dict(D=32), 5), (dict(D=96), 5), (dict(D=256), 5),
+    (dict(dtype=2), 6), (dict(dtype=7), 6),
+    (dict(scale=0.0), 7), (dict(scale=-1.0), 7), (dict(scale=float("inf")), 7), (dict(scale=float("nan")), 7),
+    (dict(o=QP + 16), 9), (dict(o=VP - 64), 9),
+])
+def test_rejects_before_any_cuda_call(lib, kw, status):
+    assert call(lib, **kw) == status
+
+
+def test_fp8_entry_checks(lib):
+    f = lib.sdpa_fwd_fp8
+    s = ctypes.c_float
+    assert f(QP, KP, VP, None, 1, 2, 2, 128, 128, 64, s(0.125), s(1), s(1), s(1), 0, None) == 1
+    assert f(QP, KP, VP, OP, 1, 2, 2, 128, 128, 64, s(0.125), s(0.0), s(1), s(1), 0, None) == 7
+    assert f(QP, KP, VP, OP, 1, 2, 2, 128, 128, 48, s(0.125), s(1), s(1), s(1), 0, None) == 5
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    st = call(lib)
+    assert st == 10
+    assert lib.sdpa_last_cuda_error() != 0
+
+
+def test_binding_rejects_cpu_tensors():
+    from scaled_dot_product_05_gb300 import sdpa_fwd
+    q = torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        sdpa_fwd(q, q, q)

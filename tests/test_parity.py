@@ -1,0 +1,146 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs, element by element at sizes the oracle finishes in
+seconds, and on sampled rows at the full benchmark sizes."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sdpa_inputs import make_qkv, sample_rows
+from tests.parity import assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from scaled_dot_product_05_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+    yield
+    from scaled_dot_product_05_gb300 import sdpa_device_error
+    assert sdpa_device_error() == 0
+
+
+def run_gpu(x, causal, scale=None, stream=None):
+    from scaled_dot_product_05_gb300 import sdpa_fwd
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+    o = sdpa_fwd(q, k, v, causal=causal, scale=scale, stream=stream)
+    torch.cuda.synchronize()
+    return o
+
+
+# (B, Hq, Hkv, Sq, Skv, D): several tiles, ragged tails, Sq != Skv, tiny and
+# degenerate shapes, MHA / GQA / MQA
+SMALL = [
+    (1, 2, 2, 128, 128, 64),
+    (1, 2, 2, 128, 128, 128),
+    (2, 4, 4, 384, 384, 64),
+    (2, 4, 2, 256, 256, 128),
+    (1, 8, 1, 300, 300, 128),
+    (1, 4, 4, 200, 77, 64),
+    (1, 4, 2, 77, 333, 128),
+    (3, 1, 1, 129, 129, 64),
+    (1, 1, 1, 1, 1, 128),
+    (1, 2, 1, 1, 500, 64),
+    (1, 2, 2, 500, 1, 128),
+    (1, 6, 3, 640, 640, 128),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_small_full_compare(shape, causal, dtype):
+    B, Hq, Hkv, Sq, Skv, D = shape
+    x = make_qkv(zlib.crc32(repr((shape, causal, dtype)).encode()) % 100000, B, Hq, Hkv, Sq, Skv, D, dtype)
+    o = run_gpu(x, causal)
+    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=causal, dtype=dtype)
+    assert_close(to_np(o), ref, dtype, f"{shape} causal={causal} {dtype}")
+
+
+def test_explicit_scale_and_stream():
+    x = make_qkv(77, 1, 4, 2, 256, 256, 128, "bf16")
+    s = torch.cuda.Stream()
+    o = run_gpu(x, True, scale=0.2, stream=s)
+    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=True, scale=0.2, dtype="bf16")
+    assert_close(to_np(o), ref, "bf16", "scale=0.2 side stream")
+
+
+def test_causal_first_row_is_v0_and_last_row_matches_full():
+    # section 7 of the codelab: position 0 sees only itself; the last sees all
+    x = make_qkv(5, 2, 4, 4, 512, 512, 64, "bf16")
+    oc, on = to_np(run_gpu(x, True)), to_np(run_gpu(x, False))
+    np.testing.assert_array_equal(oc[:, 0], x.v[:, 0].double().numpy())
+    assert np.abs(oc[:, -1] - on[:, -1]).max() <= 1e-2
+
+
+def test_gqa_matches_repeated_kv_on_gpu():
+    x = make_qkv(6, 1, 8, 2, 256, 256, 128, "bf16")
+    o_g = run_gpu(x, True)
+    x.k = x.k.repeat_interleave(4, dim=2).contiguous()
+    x.v = x.v.repeat_interleave(4, dim=2).contiguous()
+    o_m = run_gpu(x, True)
+    assert torch.equal(o_g, o_m)
+
+
+def test_deterministic():
+    x = make_qkv(8, 2, 8, 2, 1024, 1024, 128, "bf16")
+    a, b = run_gpu(x, True), run_gpu(x, True)
+    assert torch.equal(a, b)
+
+
+def test_output_guard_bands_untouched():
+    from scaled_dot_product_05_gb300 import sdpa_fwd
+    x = make_qkv(9, 1, 2, 2, 200, 200, 128, "bf16")
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+    n = q.numel()
+    buf = torch.full((n + 2 * 4096,), 12345.0, dtype=torch.bfloat16, device=dev)
+    o = buf[4096:4096 + n].view(q.shape)
+    sdpa_fwd(q, k, v, o, causal=True)
+    torch.cuda.synchronize()
+    assert (buf[:4096] == 12345.0).all() and (buf[4096 + n:] == 12345.0).all()
+    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=True, dtype="bf16")
+    assert_close(to_np(o), ref, "bf16", "guarded")
+
+
+# ---- the workload shapes, full size ----------------------------------------
+
+def sampled_check(x, causal, n_rows, seed, dtype="bf16"):
+    B, Sq, Hq, D = x.q.shape
+    o = to_np(run_gpu(x, causal)).reshape(-1, D)
+    rows = sample_rows(seed, B, Sq, Hq, n_rows)
+    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=causal, dtype=dtype, rows=rows)
+    return assert_close(o[rows], ref, dtype, f"{tuple(x.q.shape)} causal={causal}")
+
+
+def test_tiny_mha_noncausal_full():
+    x = make_qkv(0, 1, 2, 2, 128, 128, 64, "bf16")
+    o = run_gpu(x, False)
+    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=False, dtype="bf16")
+    assert_close(to_np(o), ref, "bf16", "tiny MHA")
+
+
+def test_causal_mha_1024_full():
+    x = make_qkv(1, 4, 16, 16, 1024, 1024, 64, "bf16")
+    o = run_gpu(x, True)
+    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=True, dtype="bf16")
+    assert_close(to_np(o), ref, "bf16", "causal MHA S=1024")
+
+
+def test_causal_gqa_4096_sampled():
+    x = make_qkv(2, 2, 32, 8, 4096, 4096, 128, "bf16")
+    sampled_check(x, True, 3000, 2)
+
+
+@pytest.mark.parametrize("B,S", [(64, 512), (32, 1024), (16, 2048), (8, 4096), (4, 8192), (2, 16384)])
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+def test_mqa_sweep_sampled(B, S, causal):
+    x = make_qkv(3 + S, B, 32, 1, S, S, 128, "bf16")
+    sampled_check(x, causal, 600 if S >= 8192 else 1000, 3 + S)
