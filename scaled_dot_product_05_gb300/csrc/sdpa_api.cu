@@ -50,6 +50,7 @@ struct DeviceState {
     std::once_flag once;
     cudaError_t err = cudaSuccess;
     bool arch_ok = false;
+    int sm_count = 0;
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -60,7 +61,7 @@ cudaError_t set_attrs()
                                 sdpa::Layout<D>::kSmemBytes);
 }
 
-sdpa_status_t device_ready(int* dev_out)
+sdpa_status_t device_ready(int* dev_out, int* sm_count)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -80,6 +81,11 @@ sdpa_status_t device_ready(int* dev_out)
         st.arch_ok = (major == 10 && minor == 3);
         if (!st.arch_ok)
             return;
+        cudaError_t e3 = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e3 != cudaSuccess) {
+            st.err = e3;
+            return;
+        }
         cudaError_t es[] = {set_attrs<64, true>(), set_attrs<64, false>(), set_attrs<128, true>(),
                             set_attrs<128, false>()};
         for (cudaError_t x : es)
@@ -91,6 +97,7 @@ sdpa_status_t device_ready(int* dev_out)
     if (!st.arch_ok)
         return SDPA_ERR_ARCH;
     *dev_out = dev;
+    *sm_count = st.sm_count;
     return SDPA_OK;
 }
 
@@ -123,10 +130,9 @@ sdpa_status_t check_common(const void* Q, const void* K, const void* V, const vo
         return SDPA_ERR_HEADS;
     if (s.D != 64 && s.D != 128)
         return SDPA_ERR_HEAD_DIM;
-    // grid = B * Hq * ceil(Sq / 128) CTAs must fit a 32-bit grid dimension;
-    // B * Hq must fit the kernel's int arithmetic
-    const int64_t n_qt = (static_cast<int64_t>(s.Sq) + sdpa::kBlockM - 1) / sdpa::kBlockM;
-    if (static_cast<int64_t>(s.B) * s.Hq > INT32_MAX || static_cast<int64_t>(s.B) * s.Hq * n_qt > INT32_MAX)
+    // the B * Hq * ceil(Sq / 256) work units are counted in int
+    const int64_t n_pairs = (static_cast<int64_t>(s.Sq) + sdpa::kUnitRows - 1) / sdpa::kUnitRows;
+    if (static_cast<int64_t>(s.B) * s.Hq * n_pairs > INT32_MAX)
         return SDPA_ERR_BAD_SHAPE;
     const size_t nq = static_cast<size_t>(s.B) * s.Sq * s.Hq * s.D;
     const size_t nkv = static_cast<size_t>(s.B) * s.Skv * s.Hkv * s.D;
@@ -162,9 +168,10 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
 
 template <int D, bool kBF16>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const sdpa::Params& p,
-                   cudaStream_t stream)
+                   int sm_count, cudaStream_t stream)
 {
-    const unsigned grid = static_cast<unsigned>(p.B) * p.Hq * p.n_qtiles;
+    // persistent: one CTA per SM (each takes all 512 TMEM columns)
+    const unsigned grid = static_cast<unsigned>(p.n_units < sm_count ? p.n_units : sm_count);
     sdpa::sdpa_fwd_kernel<D, kBF16><<<grid, sdpa::kThreads, sdpa::Layout<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
@@ -185,8 +192,8 @@ sdpa_status_t sdpa_fwd(const void* Q, const void* K, const void* V, void* O, int
     if (!valid_scale(scale))
         return SDPA_ERR_SCALE;
 
-    int dev = 0;
-    st = device_ready(&dev);
+    int dev = 0, sm_count = 0;
+    st = device_ready(&dev, &sm_count);
     if (st != SDPA_OK)
         return st;
 
@@ -205,7 +212,8 @@ sdpa_status_t sdpa_fwd(const void* Q, const void* K, const void* V, void* O, int
     p.Sq = Sq;
     p.Skv = Skv;
     p.group = Hq / Hkv;
-    p.n_qtiles = (Sq + sdpa::kBlockM - 1) / sdpa::kBlockM;
+    p.n_pairs = (Sq + sdpa::kUnitRows - 1) / sdpa::kUnitRows;
+    p.n_units = B * Hq * p.n_pairs;
     p.n_ktiles = (Skv + sdpa::kBlockN - 1) / sdpa::kBlockN;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
@@ -214,9 +222,9 @@ sdpa_status_t sdpa_fwd(const void* Q, const void* K, const void* V, void* O, int
     cudaError_t e;
     const bool bf16 = dtype == SDPA_DTYPE_BF16;
     if (D == 64)
-        e = bf16 ? launch<64, true>(tq, tk, tv, p, cs) : launch<64, false>(tq, tk, tv, p, cs);
+        e = bf16 ? launch<64, true>(tq, tk, tv, p, sm_count, cs) : launch<64, false>(tq, tk, tv, p, sm_count, cs);
     else
-        e = bf16 ? launch<128, true>(tq, tk, tv, p, cs) : launch<128, false>(tq, tk, tv, p, cs);
+        e = bf16 ? launch<128, true>(tq, tk, tv, p, sm_count, cs) : launch<128, false>(tq, tk, tv, p, sm_count, cs);
     if (e != cudaSuccess)
         return cuda_fail(e);
     return SDPA_OK;

@@ -7,24 +7,31 @@
 // tiling that section 8 ("Run benchmarks", sequence sweep) credits fused
 // kernels with.
 //
-// One CTA computes one work unit: 128 query rows of one (batch, query head).
-// Warp roles:
-//   warp 0      TMA producer: the Q tile once, then K_j and V_j tiles into
-//               two- or three-stage shared-memory rings.
-//   warp 1      tcgen05 issuer: S_j = Q K_j^T into one of two TMEM score
-//               buffers, and O += P_j V_j with P_j read from TMEM.
-//   warps 2..5  softmax warpgroup: one thread per query row reads its S row
-//               from TMEM, applies the causal / tail mask, updates the
-//               running max m and sum l, writes P = exp2(S*c - m) as 16-bit
-//               values back over its S row, rescales O in TMEM when m moved,
-//               and finally writes O / l to global memory.
+// Persistent kernel: one CTA per SM walks a static list of work units.  A
+// unit is 256 query rows (two 128-row Q tiles, t = 0, 1) of one (batch,
+// query head); both tiles share every K/V tile the producer brings in.
+// Warp roles (12 warps):
+//   warps 0..3   softmax warpgroup for Q tile 0
+//   warps 4..7   softmax warpgroup for Q tile 1
+//   warp 8       TMA producer: Q tiles, then K_j / V_j into shared-memory rings
+//   warp 9       tcgen05 issuer (single thread): S_t = Q_t K_j^T into TMEM and
+//                O_t += P_t V_j with P_t read from TMEM
+//   warps 10,11  idle
+// The two softmax warpgroups alternate with the tensor core: while one turns
+// S_t into P_t, the MMAs of the other tile run.  Each softmax thread owns one
+// query row: it reads its S row from TMEM, masks only the diagonal / tail
+// tile, keeps the running max m (exp2 domain) and sum l in fp32, writes
+// P = exp2(S*c - m) as 16-bit values over its S row, and rescales its O row in
+// TMEM only when m grows by more than 8 (a factor 256; P and l stay exact
+// relative to the m actually used).  After the unit's last tile it reads O_t,
+// releases the accumulator for the next unit, and stores O / l to HBM.
 //
 // Layout: Q, O are [B][Sq][Hq][D] and K, V are [B][Skv][Hkv][D] (section 3,
 // "Create Q, K and V test arrays": (B, T, N, H)).  Query head hq reads KV head
 // hq / (Hq / Hkv) (section 9, "Compare MHA, GQA and MQA"); nothing is
 // replicated.  Causal masking keeps the lower triangle (section 7, "Add causal
 // masking"): row i sees keys 0..i; key tiles wholly above the diagonal are
-// skipped and only the diagonal tile is masked element-wise.
+// skipped.
 #pragma once
 
 #include <cstdint>
@@ -36,10 +43,20 @@
 
 namespace sdpa {
 
-constexpr int kBlockM = 128;         // query rows per work unit (= TMEM lanes)
+constexpr int kBlockM = 128;         // query rows per Q tile (= TMEM lanes)
 constexpr int kBlockN = 128;         // keys per K/V tile
-constexpr int kThreads = 192;        // 6 warps
+constexpr int kUnitRows = 2 * kBlockM;
+constexpr int kThreads = 384;        // 12 warps
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+// Register split: launched at 168 per thread (384 x 168 = 64512); the
+// producer warpgroup (warps 8..11) drops to 104 and the two softmax warpgroups
+// rise to 192: 128 x 104 + 256 x 192 = 62464 <= 64512.
+constexpr uint32_t kRegsProducer = 104;
+constexpr uint32_t kRegsSoftmax = 192;
+static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * 168, "register split exceeds the launch budget");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per barrier wait
+constexpr float kRescaleThreshold = 8.0f;          // log2 units: rescale O when m grows by > 2^8
 
 // Device error word: 0 = no error; otherwise the first failure recorded by any
 // CTA (see the codes below).  Read and cleared by the host through the C-ABI.
@@ -55,7 +72,8 @@ struct Params {
     void* O;
     int B, Hq, Hkv, Sq, Skv;
     int group;                       // Hq / Hkv
-    int n_qtiles;                    // ceil(Sq / 128)
+    int n_units;                     // B * Hq * n_pairs
+    int n_pairs;                     // ceil(Sq / 256)
     int n_ktiles;                    // ceil(Skv / 128)
     int causal;
     float scale_log2;                // scale * log2(e): scores enter exp2
@@ -66,33 +84,32 @@ struct Layout {
     static constexpr int kChunks = D / 64;                   // 128-byte swizzle column blocks
     static constexpr int kChunkBytes = kBlockM * 128;         // 128 rows x 128 B
     static constexpr int kTileBytes = kBlockM * D * 2;        // one Q, K or V tile
-    static constexpr int kStages = (D == 128) ? 2 : 3;
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kTileBytes;
-    static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-    static constexpr int kBarBytes = 512;
-    // Request at least ~116 KB so that only one CTA (which takes all 512 TMEM
-    // columns) is resident per SM.
-    static constexpr int kUsed = kOffBar + kBarBytes;
-    static constexpr int kSmemBytes = (kUsed > 118 * 1024 ? kUsed : 118 * 1024) + 1024;
+    static constexpr int kStagesK = (D == 128) ? 3 : 4;
+    static constexpr int kStagesV = (D == 128) ? 2 : 4;
+    static constexpr int kOffQ = 0;                           // Q tile 0, Q tile 1
+    static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+    static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
+    static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
+    static constexpr int kBarBytes = 1024;
+    static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + alignment slack
     // TMEM columns
-    static constexpr uint32_t kTmemS0 = 0;
-    static constexpr uint32_t kTmemS1 = 128;
-    static constexpr uint32_t kTmemO = 256;
+    __host__ __device__ static constexpr uint32_t tmem_s(int t) { return 128u * t; }        // S_t / P_t
+    __host__ __device__ static constexpr uint32_t tmem_o(int t) { return 256u + 128u * t; } // O_t
     static constexpr uint32_t kTmemCols = 512;
 };
 
-template <int kStages>
+template <int NK, int NV>
 struct Barriers {
-    uint64_t q_full;
-    uint64_t k_full[kStages];
-    uint64_t k_empty[kStages];
-    uint64_t v_full[kStages];
-    uint64_t v_empty[kStages];
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
+    uint64_t k_full[NK];
+    uint64_t k_empty[NK];
+    uint64_t v_full[NV];
+    uint64_t v_empty[NV];
     uint64_t s_full[2];
     uint64_t p_full[2];
-    uint64_t o_done;
+    uint64_t o_full[2];
+    uint64_t o_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -119,6 +136,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
+// Waits without recording an error (used only to drain in-flight work after
+// an abort).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
+    }
+}
+
 template <bool kBF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
@@ -131,59 +157,95 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     }
 }
 
+// Work unit -> (b, hq, pair).  Causal units are ordered heaviest first (the
+// last query rows see the most keys).
+struct Unit {
+    int b, hq, hkv, pair;
+    int n_kv[2];                     // key tiles visited by Q tile 0 / 1
+};
+
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u)
+{
+    Unit w;
+    const int bh_count = p.B * p.Hq;
+    w.pair = u / bh_count;
+    if (p.causal)
+        w.pair = p.n_pairs - 1 - w.pair;
+    const int bh = u % bh_count;
+    w.b = bh / p.Hq;
+    w.hq = bh % p.Hq;
+    w.hkv = w.hq / p.group;
+    if (p.causal) {
+        w.n_kv[0] = min(p.n_ktiles, 2 * w.pair + 1);
+        w.n_kv[1] = min(p.n_ktiles, 2 * w.pair + 2);
+    } else {
+        w.n_kv[0] = w.n_kv[1] = p.n_ktiles;
+    }
+    return w;
+}
+
+// Static schedule: CTA c takes, in round r, unit r*G + c (r even) or
+// r*G + G-1-c (r odd), G = gridDim.x.  With units sorted heaviest first this
+// zig-zag pairs heavy and light causal units on every CTA.  Returns -1 when
+// the CTA has no unit in round r (only possible in the last round) and -2
+// once the rounds are exhausted.
+__device__ __forceinline__ int unit_of_round(const Params& p, int r)
+{
+    const int G = gridDim.x;
+    const int base = r * G;
+    if (base >= p.n_units)
+        return -2;
+    const int u = base + ((r & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    return u < p.n_units ? u : -1;
+}
+
 template <int D, bool kBF16>
 __global__ void __launch_bounds__(kThreads, 1)
 sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const Params p)
 {
     using L = Layout<D>;
-    constexpr int NS = L::kStages;
+    constexpr int NK = L::kStagesK;
+    constexpr int NV = L::kStagesV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    auto* bars = reinterpret_cast<Barriers<NS>*>(smem + L::kOffBar);
+    auto* bars = reinterpret_cast<Barriers<NK, NV>*>(smem + L::kOffBar);
     volatile int* abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- work unit: heaviest causal tiles (largest q-tile index) first ------
-    const int bh_count = p.B * p.Hq;
-    int qt = blockIdx.x / bh_count;
-    if (p.causal)
-        qt = p.n_qtiles - 1 - qt;
-    const int bh = blockIdx.x % bh_count;
-    const int b = bh / p.Hq;
-    const int hq = bh % p.Hq;
-    const int hkv = hq / p.group;
-    const int n_kv = p.causal ? min(p.n_ktiles, qt + 1) : p.n_ktiles;
 
     const uint32_t sQ = smem_u32(smem + L::kOffQ);
     const uint32_t sK = smem_u32(smem + L::kOffK);
     const uint32_t sV = smem_u32(smem + L::kOffV);
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bars->q_full), 1);
-        for (int s = 0; s < NS; ++s) {
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(smem_u32(&bars->q_full[t]), 1);
+            mbar_init(smem_u32(&bars->q_empty[t]), 1);
+            mbar_init(smem_u32(&bars->s_full[t]), 1);
+            mbar_init(smem_u32(&bars->p_full[t]), 128);
+            mbar_init(smem_u32(&bars->o_full[t]), 1);
+            mbar_init(smem_u32(&bars->o_empty[t]), 128);
+        }
+        for (int s = 0; s < NK; ++s) {
             mbar_init(smem_u32(&bars->k_full[s]), 1);
             mbar_init(smem_u32(&bars->k_empty[s]), 1);
+        }
+        for (int s = 0; s < NV; ++s) {
             mbar_init(smem_u32(&bars->v_full[s]), 1);
             mbar_init(smem_u32(&bars->v_empty[s]), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&bars->s_full[i]), 1);
-            mbar_init(smem_u32(&bars->p_full[i]), 128);
-        }
-        mbar_init(smem_u32(&bars->o_done), 1);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_map(&tm_q);
         tma_prefetch_map(&tm_k);
         tma_prefetch_map(&tm_v);
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&bars->tmem_base), L::kTmemCols);
         tmem_relinquish();
     }
@@ -192,215 +254,324 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 0) {
+    if (warp >= 8) {
+      regs_release<kRegsProducer>();
+      if (warp == kProducerWarp) {
         // =========================== TMA producer ===========================
         if (lane == 0) {
-            const int q0 = qt * kBlockM;
-            mbar_arrive_expect_tx(smem_u32(&bars->q_full), L::kTileBytes);
-            for (int c = 0; c < L::kChunks; ++c)
-                tma_load_4d(sQ + c * L::kChunkBytes, &tm_q, smem_u32(&bars->q_full), c * 64, hq, q0, b);
-            int nk = 0, nv = 0;                              // K / V tiles issued
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % NS;
-                const uint32_t par = ((j / NS) & 1) ^ 1;     // phase of the release of tile j - NS
-                if (j >= NS && !wait_bar(smem_u32(&bars->k_empty[s]), par, abort, kErrWaitLoad + 1))
-                    break;
+            uint32_t nk = 0, nv = 0;             // K / V tiles issued (ring position)
+            uint32_t nq[2] = {0, 0};             // Q tiles issued per slot
+            bool ok = true;
+            auto load_q = [&](const Unit& w, int t) -> bool {
+                if (nq[t] > 0 && !wait_bar(smem_u32(&bars->q_empty[t]), (nq[t] - 1) & 1, abort, kErrWaitLoad + 1 + t))
+                    return false;
+                mbar_arrive_expect_tx(smem_u32(&bars->q_full[t]), L::kTileBytes);
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_4d(sQ + t * L::kTileBytes + c * L::kChunkBytes, &tm_q, smem_u32(&bars->q_full[t]),
+                                c * 64, w.hq, w.pair * kUnitRows + t * kBlockM, w.b);
+                ++nq[t];
+                return true;
+            };
+            auto load_k = [&](const Unit& w, int j) -> bool {
+                const uint32_t s = nk % NK;
+                if (nk >= NK && !wait_bar(smem_u32(&bars->k_empty[s]), ((nk / NK) & 1) ^ 1, abort, kErrWaitLoad + 3))
+                    return false;
                 mbar_arrive_expect_tx(smem_u32(&bars->k_full[s]), L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_4d(sK + s * L::kTileBytes + c * L::kChunkBytes, &tm_k, smem_u32(&bars->k_full[s]),
-                                c * 64, hkv, j * kBlockN, b);
-                nk = j + 1;
-                if (j >= NS && !wait_bar(smem_u32(&bars->v_empty[s]), par, abort, kErrWaitLoad + 2))
-                    break;
+                                c * 64, w.hkv, j * kBlockN, w.b);
+                ++nk;
+                return true;
+            };
+            auto load_v = [&](const Unit& w, int j) -> bool {
+                const uint32_t s = nv % NV;
+                if (nv >= NV && !wait_bar(smem_u32(&bars->v_empty[s]), ((nv / NV) & 1) ^ 1, abort, kErrWaitLoad + 4))
+                    return false;
                 mbar_arrive_expect_tx(smem_u32(&bars->v_full[s]), L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_4d(sV + s * L::kTileBytes + c * L::kChunkBytes, &tm_v, smem_u32(&bars->v_full[s]),
-                                c * 64, hkv, j * kBlockN, b);
-                nv = j + 1;
+                                c * 64, w.hkv, j * kBlockN, w.b);
+                ++nv;
+                return true;
+            };
+            for (int r = 0; ok; ++r) {
+                const int u = unit_of_round(p, r);
+                if (u == -2)
+                    break;
+                if (u < 0)
+                    continue;
+                const Unit w = decode_unit(p, u);
+                const int n = w.n_kv[1];
+                ok = load_q(w, 0) && load_k(w, 0) && load_q(w, 1) && load_v(w, 0);
+                for (int j = 1; ok && j < n; ++j)
+                    ok = load_k(w, j) && load_v(w, j);
             }
-            // Never leave the CTA with copies in flight: after an abort, wait
-            // (bounded) for the last copy issued into every stage.
             if (*abort) {
-                auto drain = [&](uint32_t bar, uint32_t parity) {
-                    const uint64_t t0 = global_timer_ns();
-                    while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
-                    }
-                };
-                drain(smem_u32(&bars->q_full), 0);
-                for (int j = (nk > NS ? nk - NS : 0); j < nk; ++j)
-                    drain(smem_u32(&bars->k_full[j % NS]), (j / NS) & 1);
-                for (int j = (nv > NS ? nv - NS : 0); j < nv; ++j)
-                    drain(smem_u32(&bars->v_full[j % NS]), (j / NS) & 1);
+                // never leave the CTA with copies in flight
+                for (int t = 0; t < 2; ++t)
+                    if (nq[t] > 0)
+                        drain_wait(smem_u32(&bars->q_full[t]), (nq[t] - 1) & 1);
+                for (uint32_t i = (nk > NK ? nk - NK : 0); i < nk; ++i)
+                    drain_wait(smem_u32(&bars->k_full[i % NK]), (i / NK) & 1);
+                for (uint32_t i = (nv > NV ? nv - NV : 0); i < nv; ++i)
+                    drain_wait(smem_u32(&bars->v_full[i % NV]), (i / NV) & 1);
             }
         }
-    } else if (warp == 1) {
+      } else if (warp == kMmaWarp) {
         // ============================ MMA issuer ============================
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f16(kBF16, kBlockM, kBlockN, false);
             constexpr uint32_t idesc_o = idesc_f16(kBF16, kBlockM, D, true);
-            bool ok = wait_bar(smem_u32(&bars->q_full), 0, abort, kErrWaitMma + 0);
-            tc_fence_after_sync();
-            // S_j = Q K_j^T into score buffer j & 1.  Q and K tiles are K-major,
-            // 128-byte swizzled: 16-element K steps advance 32 bytes inside a
-            // 64-column block, blocks are kChunkBytes apart, 8-row groups 1024 B.
-            auto issue_s = [&](int j) -> bool {
-                const int s = j % NS;
-                if (!wait_bar(smem_u32(&bars->k_full[s]), (j / NS) & 1, abort, kErrWaitMma + 1))
-                    return false;
-                tc_fence_after_sync();
-                const uint32_t d_tmem = tmem + ((j & 1) ? L::kTmemS1 : L::kTmemS0);
-                const uint32_t kbase = sK + s * L::kTileBytes;
+            uint32_t ck = 0, cv = 0;             // K / V tiles consumed (ring position)
+            uint32_t cs[2] = {0, 0};             // S tiles issued per Q slot
+            uint32_t units = 0;
+            bool ok = true;
+
+            // S_t = Q_t K^T for the K tile at ring position `kpos`.  Q and K
+            // tiles are K-major, 128-byte swizzled: a 16-element K step moves
+            // 32 bytes inside a 64-column block, blocks are kChunkBytes apart,
+            // 8-row groups 1024 bytes apart.
+            auto issue_s = [&](int t, uint32_t kpos) {
+                const uint32_t d_tmem = tmem + L::tmem_s(t);
+                const uint32_t qbase = sQ + t * L::kTileBytes;
+                const uint32_t kbase = sK + (kpos % NK) * L::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-                    mma_f16_ss(d_tmem, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024),
+                    mma_f16_ss(d_tmem, smem_desc_sw128(qbase + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024),
                                idesc_s, kk > 0);
                 }
-                mma_commit(smem_u32(&bars->s_full[j & 1]));
-                mma_commit(smem_u32(&bars->k_empty[s]));
-                return true;
+                mma_commit(smem_u32(&bars->s_full[t]));
+                ++cs[t];
             };
-            if (ok && n_kv > 0)
-                ok = issue_s(0);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv && !issue_s(j + 1))
-                    break;
-                const int buf = j & 1;
-                if (!wait_bar(smem_u32(&bars->p_full[buf]), (j >> 1) & 1, abort, kErrWaitMma + 2))
-                    break;
-                tc_fence_after_sync();
-                const int s = j % NS;
-                if (!wait_bar(smem_u32(&bars->v_full[s]), (j / NS) & 1, abort, kErrWaitMma + 3))
-                    break;
-                tc_fence_after_sync();
-                // O += P_j V_j.  P: 128 x 128 16-bit in TMEM (8 columns per
-                // 16 keys).  V tile is MN-major (D contiguous), 128-byte
-                // swizzled: 16 keys = 2048 B; the next 64 columns of D are one
-                // chunk (kChunkBytes) further.
-                const uint32_t p_tmem = tmem + (buf ? L::kTmemS1 : L::kTmemS0);
-                const uint32_t vbase = sV + s * L::kTileBytes;
+            // O_t (+)= P_t V for the V tile at ring position `vpos`.  P_t is
+            // 128 x 128 16-bit in TMEM (8 columns per 16 keys); the V tile is
+            // MN-major (D contiguous), 128-byte swizzled: 16 keys = 2048 bytes,
+            // the next 64 columns of D one chunk further.
+            auto issue_pv = [&](int t, uint32_t vpos, bool accumulate) {
+                const uint32_t p_tmem = tmem + L::tmem_s(t);
+                const uint32_t vbase = sV + (vpos % NV) * L::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    mma_f16_ts(tmem + L::kTmemO, p_tmem + kk * 8,
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    mma_f16_ts(tmem + L::tmem_o(t), p_tmem + kk * 8,
                                smem_desc_sw128(vbase + kk * 2048, L::kChunkBytes, 1024), idesc_o,
-                               (j > 0 || kk > 0) ? 1u : 0u);
+                               (accumulate || kk > 0) ? 1u : 0u);
+            };
+            auto wait_k = [&](uint32_t kpos) {
+                return wait_bar(smem_u32(&bars->k_full[kpos % NK]), (kpos / NK) & 1, abort, kErrWaitMma + 3);
+            };
+
+            for (int r = 0; ok; ++r) {
+                const int u = unit_of_round(p, r);
+                if (u == -2)
+                    break;
+                if (u < 0)
+                    continue;
+                const Unit w = decode_unit(p, u);
+                const int n = w.n_kv[1];         // tile 1 visits at least as many key tiles as tile 0
+                // first K tile: S_0 for both Q tiles
+                ok = wait_k(ck);
+                for (int t = 0; ok && t < 2; ++t) {
+                    ok = wait_bar(smem_u32(&bars->q_full[t]), units & 1, abort, kErrWaitMma + 1 + t);
+                    if (!ok)
+                        break;
+                    tc_fence_after_sync();
+                    issue_s(t, ck);
+                    if (w.n_kv[t] == 1)
+                        mma_commit(smem_u32(&bars->q_empty[t]));
                 }
-                mma_commit(smem_u32(&bars->v_empty[s]));
-                mma_commit(smem_u32(&bars->o_done));
+                if (!ok)
+                    break;
+                mma_commit(smem_u32(&bars->k_empty[ck % NK]));
+                ++ck;
+                for (int j = 0; ok && j < n; ++j) {
+                    // V_j is used by both Q tiles (tile 0 only while j < n0)
+                    ok = wait_bar(smem_u32(&bars->v_full[cv % NV]), (cv / NV) & 1, abort, kErrWaitMma + 5);
+                    if (!ok)
+                        break;
+                    const bool more = j + 1 < n;
+                    bool k_ready = false;            // K_{j+1} waited for
+                    for (int t = 0; t < 2; ++t) {
+                        if (j >= w.n_kv[t])
+                            continue;
+                        ok = wait_bar(smem_u32(&bars->p_full[t]), (cs[t] - 1) & 1, abort, kErrWaitMma + 6 + t);
+                        if (ok && j == 0 && units > 0)
+                            ok = wait_bar(smem_u32(&bars->o_empty[t]), (units - 1) & 1, abort, kErrWaitMma + 8 + t);
+                        if (!ok)
+                            break;
+                        tc_fence_after_sync();
+                        issue_pv(t, cv, j > 0);
+                        if (j == w.n_kv[t] - 1)
+                            mma_commit(smem_u32(&bars->o_full[t]));
+                        // next S_t over the same TMEM columns: ordered after this P V
+                        if (j + 1 < w.n_kv[t]) {
+                            if (!k_ready && !(ok = k_ready = wait_k(ck)))
+                                break;
+                            issue_s(t, ck);
+                            if (j + 2 == w.n_kv[t])
+                                mma_commit(smem_u32(&bars->q_empty[t]));
+                        }
+                    }
+                    if (!ok)
+                        break;
+                    mma_commit(smem_u32(&bars->v_empty[cv % NV]));
+                    ++cv;
+                    if (more) {
+                        mma_commit(smem_u32(&bars->k_empty[ck % NK]));
+                        ++ck;
+                    }
+                }
+                ++units;
             }
-            // Every MMA this thread issued completes before TMEM is released.
+            // every MMA this thread issued completes before TMEM is released
             mma_commit(smem_u32(&bars->drain));
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(smem_u32(&bars->drain), 0) && global_timer_ns() - t0 < kWaitLimitNs) {
-            }
+            drain_wait(smem_u32(&bars->drain), 0);
         }
+      }
     } else {
-        // ========================= softmax warpgroup ========================
+        regs_acquire<kRegsSoftmax>();
+        // ========================= softmax warpgroups =======================
+        const int t = warp >> 2;                           // Q tile of this warpgroup
         const int quarter = warp & 3;                      // TMEM lanes 32*quarter ..
         const int row = quarter * 32 + lane;
-        const int q_idx = qt * kBlockM + row;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const uint32_t s_tmem = tmem + lane_addr + L::tmem_s(t);
+        const uint32_t o_tmem = tmem + lane_addr + L::tmem_o(t);
         const float c = p.scale_log2;
-        int limit = p.Skv - 1;                             // last visible key of this row
-        if (p.causal && q_idx < limit)
-            limit = q_idx;
-        float m = -INFINITY;                               // running max of S*c
-        float l = 0.f;                                     // running sum of exp2(S*c - m)
+        uint32_t cs = 0;                                   // S tiles consumed
+        uint32_t units = 0;
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const int buf = j & 1;
-            const uint32_t s_tmem = tmem + lane_addr + (buf ? L::kTmemS1 : L::kTmemS0);
-            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full[buf]), (j >> 1) & 1, abort,
-                                                  kErrWaitSoftmax + 1));
+        for (int r = 0; ok; ++r) {
+            const int u = unit_of_round(p, r);
+            if (u == -2)
+                break;
+            if (u < 0)
+                continue;
+            const Unit w = decode_unit(p, u);
+            const int n = w.n_kv[t];
+            const int q_idx = w.pair * kUnitRows + t * kBlockM + row;
+            int limit = p.Skv - 1;                         // last key this row sees
+            if (p.causal && q_idx < limit)
+                limit = q_idx;
+            float m = -INFINITY;                           // running max of S*c
+            float l = 0.f;                                 // running sum of exp2(S*c - m)
+            for (int j = 0; j < n; ++j) {
+                ok = __all_sync(0xffffffffu,
+                                wait_bar(smem_u32(&bars->s_full[t]), cs & 1, abort, kErrWaitSoftmax + 1 + t));
+                if (!ok)
+                    break;
+                ++cs;
+                tc_fence_after_sync();
+                uint32_t r[128];
+                tmem_ld128_wait(s_tmem, s_tmem + 32, s_tmem + 64, s_tmem + 96, r);
+                const int k0 = j * kBlockN;
+                if (k0 + kBlockN - 1 > limit) {
+#pragma unroll
+                    for (int i = 0; i < 128; ++i)
+                        if (k0 + i > limit)
+                            r[i] = 0xff800000u;            // -inf
+                }
+                // row max: four chains of three-operand max
+                float mx0 = __uint_as_float(r[0]), mx1 = __uint_as_float(r[1]);
+                float mx2 = __uint_as_float(r[2]), mx3 = __uint_as_float(r[3]);
+#pragma unroll
+                for (int i = 4; i < 124; i += 8) {              // elements 4..123
+                    mx0 = fmax3(mx0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                    mx1 = fmax3(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                    mx2 = fmax3(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+                    mx3 = fmax3(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+                }
+                mx0 = fmax3(mx0, __uint_as_float(r[124]), __uint_as_float(r[125]));
+                mx1 = fmax3(mx1, __uint_as_float(r[126]), __uint_as_float(r[127]));
+                const float m_tile = fmax3(fmaxf(mx0, mx1), mx2, mx3) * c;
+                float alpha = 1.f;
+                bool rescale = false;
+                if (j == 0) {
+                    m = m_tile;
+                } else if (m_tile > m + kRescaleThreshold) {
+                    alpha = ex2_approx(m - m_tile);
+                    m = m_tile;
+                    rescale = true;
+                }
+                // P = exp2(S*c - m): packed FMA for the argument, packed adds
+                // for the row sum
+                const uint64_t c2 = f32x2(c, c);
+                const uint64_t nm2 = f32x2(-m, -m);
+                uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int e = 64 * h + 2 * i;
+                        float x0, x1;
+                        f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2), x0, x1);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        if (i & 1)
+                            acc1 = add_f32x2(acc1, f32x2(p0, p1));
+                        else
+                            acc0 = add_f32x2(acc0, f32x2(p0, p1));
+                        pk[i] = pack2<kBF16>(p0, p1);
+                    }
+                    tmem_st32(s_tmem + 32 * h, pk);
+                }
+                float sa, sb;
+                f32x2_split(add_f32x2(acc0, acc1), sa, sb);
+                const float sum0 = sa, sum1 = sb;
+                l = l * alpha + (sum0 + sum1);
+                // O_t holds the sum up to tile j-1 (its last P V completed before
+                // S_t(j) did); rescale it before P_t(j) V_j accumulates.
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_ld32_wait(o_tmem + cc * 32, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(o_tmem + cc * 32, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(smem_u32(&bars->p_full[t]));
+            }
+            if (!ok)
+                break;
+            // ---- epilogue: O_t / l -> 16-bit -> HBM -------------------------
+            ok = __all_sync(0xffffffffu,
+                            wait_bar(smem_u32(&bars->o_full[t]), units & 1, abort, kErrWaitSoftmax + 3 + t));
             if (!ok)
                 break;
             tc_fence_after_sync();
-            uint32_t r[128];
-            tmem_ld128_wait(s_tmem, s_tmem + 32, s_tmem + 64, s_tmem + 96, r);
-            float sv[128];
-#pragma unroll
-            for (int i = 0; i < 128; ++i)
-                sv[i] = __uint_as_float(r[i]);
-            const int k0 = j * kBlockN;
-            if (k0 + kBlockN - 1 > limit) {
-#pragma unroll
-                for (int i = 0; i < 128; ++i)
-                    if (k0 + i > limit)
-                        sv[i] = -INFINITY;
+            uint32_t o[D];
+            if constexpr (D == 128) {
+                tmem_ld128_wait(o_tmem, o_tmem + 32, o_tmem + 64, o_tmem + 96, o);
+            } else {
+                tmem_ld32_wait(o_tmem, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+                tmem_ld32_wait(o_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
             }
-            float mt = sv[0];
-#pragma unroll
-            for (int i = 1; i < 128; ++i)
-                mt = fmaxf(mt, sv[i]);
-            const float m_new = fmaxf(m, mt * c);
-            const float alpha = ex2_approx(m - m_new);     // 0 on the first tile
-            float sum = 0.f;
-            uint32_t pk[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const float p0 = ex2_approx(fmaf(sv[2 * i], c, -m_new));
-                const float p1 = ex2_approx(fmaf(sv[2 * i + 1], c, -m_new));
-                sum += p0 + p1;
-                pk[i] = pack2<kBF16>(p0, p1);
-            }
-            l = l * alpha + sum;
-            m = m_new;
-            tmem_st32(s_tmem, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-            tmem_st32(s_tmem + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-            // Rescale O by alpha once P_{j-1} V_{j-1} has landed (any row of
-            // the warp that moved its max makes the warp do it).
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                ok = __all_sync(0xffffffffu,
-                                wait_bar(smem_u32(&bars->o_done), (j - 1) & 1, abort, kErrWaitSoftmax + 2));
-                if (!ok)
-                    break;
-                tc_fence_after_sync();
-#pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t o[32];
-                    const uint32_t o_tmem = tmem + lane_addr + L::kTmemO + cc * 32;
-                    tmem_ld32_wait(o_tmem, o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(o_tmem, o);
-                }
-            }
-            tmem_st_wait();
             tc_fence_before_sync();
-            mbar_arrive(smem_u32(&bars->p_full[buf]));
-        }
-        // ---- epilogue: O / l -> 16-bit -> global ---------------------------
-        if (ok) {
-            ok = __all_sync(0xffffffffu,
-                            wait_bar(smem_u32(&bars->o_done), (n_kv - 1) & 1, abort, kErrWaitSoftmax + 3));
-        }
-        if (ok) {
-            tc_fence_after_sync();
-            const float inv_l = 1.f / l;
-            uint8_t* out = reinterpret_cast<uint8_t*>(p.O) +
-                           (((int64_t)b * p.Sq + q_idx) * p.Hq + hq) * (int64_t)(D * 2);
+            mbar_arrive(smem_u32(&bars->o_empty[t]));
+            if (q_idx < p.Sq) {
+                const float inv_l = 1.f / l;
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.O) +
+                                                      (((int64_t)w.b * p.Sq + q_idx) * p.Hq + w.hq) * (int64_t)(D * 2));
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                tmem_ld32_wait(tmem + lane_addr + L::kTmemO + cc * 32, o);
-                uint32_t h[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    h[i] = pack2<kBF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-                if (q_idx < p.Sq) {
-                    uint4* dst = reinterpret_cast<uint4*>(out + cc * 64);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
-                }
+                for (int v = 0; v < D / 8; ++v)
+                    dst[v] = make_uint4(pack2<kBF16>(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
+                                        pack2<kBF16>(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l),
+                                        pack2<kBF16>(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l),
+                                        pack2<kBF16>(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l));
             }
+            ++units;
         }
     }
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after_sync();
         tmem_dealloc(tmem, L::kTmemCols);
