@@ -7,6 +7,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 namespace sdpa {
 
@@ -137,6 +138,33 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+// Same two forms for kind::f8f6f4 (8-bit E4M3 operands here, fp32 accumulate).
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+        "}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n"
+        "}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
@@ -152,26 +180,37 @@ __device__ __forceinline__ void tmem_st_wait()
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (all >> 4), the fixed version bits 46..48 = 0b001 and the
-// swizzle mode in bits 61..63 (2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+// swizzle mode in bits 61..63 (2 = 128-byte swizzle, 4 = 64-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t swizzle_code)
 {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
     d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= (uint64_t)(swizzle_code & 7u) << 61;
     return d;
 }
 
-// Instruction descriptor, kind::f16 with an fp32 accumulator.
-// bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
-// 1 = bf16), 15/16 A/B major-ness (0 = K-major, 1 = MN-major), 17-22 N >> 3,
-// 24-28 M >> 4.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+{
+    return smem_desc(saddr, lbo_bytes, sbo_bytes, 2u);
+}
+
+// Instruction descriptor with an fp32 accumulator (same layout for kind::f16
+// and kind::f8f6f4): bits 4-5 D format (1 = f32), 7-9 A format and 10-12
+// B format (kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3), 15/16 A/B
+// major-ness (0 = K-major, 1 = MN-major), 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_make(uint32_t ab_format, int M, int N, bool b_mn_major)
+{
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b_mn_major)
 {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+    return idesc_make(bf16 ? 1u : 0u, M, N, b_mn_major);
 }
 
 // TMEM loads (32 lanes x 32 bits, lane = thread of the warp) and stores; the
@@ -254,6 +293,36 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b)
     uint64_t d;
     asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+
+// Two floats -> two E4M3 bytes (round to nearest even, saturate to +-448):
+// `lo` in the low byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi)
+{
+    uint16_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
+    return h;
+}
+
+// Two E4M3 bytes -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t add_f16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t v)
+{
+    __half2 h = *reinterpret_cast<__half2*>(&v);
+    return __half22float2(h);
 }
 
 __device__ __forceinline__ float ex2_approx(float x)

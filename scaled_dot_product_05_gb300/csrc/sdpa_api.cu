@@ -54,11 +54,11 @@ struct DeviceState {
 };
 DeviceState g_dev[kMaxDevices];
 
-template <int D, bool kBF16>
+template <int D, int KIND>
 cudaError_t set_attrs()
 {
-    return cudaFuncSetAttribute(sdpa::sdpa_fwd_kernel<D, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                sdpa::Layout<D>::kSmemBytes);
+    return cudaFuncSetAttribute(sdpa::sdpa_fwd_kernel<D, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                sdpa::Layout<D, KIND>::kSmemBytes);
 }
 
 sdpa_status_t device_ready(int* dev_out, int* sm_count)
@@ -86,8 +86,9 @@ sdpa_status_t device_ready(int* dev_out, int* sm_count)
             st.err = e3;
             return;
         }
-        cudaError_t es[] = {set_attrs<64, true>(), set_attrs<64, false>(), set_attrs<128, true>(),
-                            set_attrs<128, false>()};
+        cudaError_t es[] = {set_attrs<64, sdpa::kBF16>(),  set_attrs<64, sdpa::kFP16>(),
+                            set_attrs<64, sdpa::kE4M3>(),  set_attrs<128, sdpa::kBF16>(),
+                            set_attrs<128, sdpa::kFP16>(), set_attrs<128, sdpa::kE4M3>()};
         for (cudaError_t x : es)
             if (x != cudaSuccess && st.err == cudaSuccess)
                 st.err = x;
@@ -149,31 +150,62 @@ bool valid_scale(float x)
 }
 
 // 4-D tensor map over a [B][S][H][D] array: dims (innermost first) {D, H, S, B},
-// box {64 elements (128 bytes), 1 head, 128 rows, 1 batch}, 128-byte swizzle,
-// zero fill out of bounds (ragged sequence tails).
+// box {one swizzle chunk of the row (128 bytes, or 64 when a row is 64 bytes),
+// 1 head, 128 rows, 1 batch}, matching swizzle, zero fill out of bounds
+// (ragged sequence tails).
 bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int D, int H, int S, int B)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
         return false;
+    const int row_bytes = D * elem_bytes;
+    const int swz = row_bytes < 128 ? row_bytes : 128;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)D * elem_bytes, (cuuint64_t)H * D * elem_bytes,
                                    (cuuint64_t)S * H * D * elem_bytes};
-    const cuuint32_t box[4] = {(cuuint32_t)(128 / elem_bytes), 1, (cuuint32_t)sdpa::kBlockM, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)(swz / elem_bytes), 1, (cuuint32_t)sdpa::kBlockM, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kBF16>
+template <int D, int KIND>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const sdpa::Params& p,
                    int sm_count, cudaStream_t stream)
 {
     // persistent: one CTA per SM (each takes all 512 TMEM columns)
     const unsigned grid = static_cast<unsigned>(p.n_units < sm_count ? p.n_units : sm_count);
-    sdpa::sdpa_fwd_kernel<D, kBF16><<<grid, sdpa::kThreads, sdpa::Layout<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
+    sdpa::sdpa_fwd_kernel<D, KIND><<<grid, sdpa::kThreads, sdpa::Layout<D, KIND>::kSmemBytes, stream>>>(tq, tk, tv,
+                                                                                                          p);
     return cudaGetLastError();
+}
+
+sdpa::Params make_params(void* O, const Shape& s, double score_scale, float out_scale, int causal)
+{
+    sdpa::Params p{};
+    p.O = O;
+    p.B = s.B;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.Sq = s.Sq;
+    p.Skv = s.Skv;
+    p.group = s.Hq / s.Hkv;
+    p.n_pairs = (s.Sq + sdpa::kUnitRows - 1) / sdpa::kUnitRows;
+    p.n_units = s.B * s.Hq * p.n_pairs;
+    p.n_ktiles = (s.Skv + sdpa::kBlockN - 1) / sdpa::kBlockN;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = static_cast<float>(score_scale * 1.4426950408889634);   // exp(x) = exp2(x log2 e)
+    p.out_scale = out_scale;
+    return p;
+}
+
+template <int KIND>
+cudaError_t launch_kind(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const sdpa::Params& p, int sm_count, cudaStream_t stream)
+{
+    return D == 64 ? launch<64, KIND>(tq, tk, tv, p, sm_count, stream)
+                   : launch<128, KIND>(tq, tk, tv, p, sm_count, stream);
 }
 
 }  // namespace
@@ -204,27 +236,10 @@ sdpa_status_t sdpa_fwd(const void* Q, const void* K, const void* V, void* O, int
         !make_map(&tv, V, dt, 2, D, Hkv, Skv, B))
         return cuda_fail(cudaErrorInvalidValue);
 
-    sdpa::Params p{};
-    p.O = O;
-    p.B = B;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.Sq = Sq;
-    p.Skv = Skv;
-    p.group = Hq / Hkv;
-    p.n_pairs = (Sq + sdpa::kUnitRows - 1) / sdpa::kUnitRows;
-    p.n_units = B * Hq * p.n_pairs;
-    p.n_ktiles = (Skv + sdpa::kBlockN - 1) / sdpa::kBlockN;
-    p.causal = causal ? 1 : 0;
-    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-
+    const sdpa::Params p = make_params(O, s, scale, 1.f, causal);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    const bool bf16 = dtype == SDPA_DTYPE_BF16;
-    if (D == 64)
-        e = bf16 ? launch<64, true>(tq, tk, tv, p, sm_count, cs) : launch<64, false>(tq, tk, tv, p, sm_count, cs);
-    else
-        e = bf16 ? launch<128, true>(tq, tk, tv, p, sm_count, cs) : launch<128, false>(tq, tk, tv, p, sm_count, cs);
+    const cudaError_t e = dtype == SDPA_DTYPE_BF16 ? launch_kind<sdpa::kBF16>(D, tq, tk, tv, p, sm_count, cs)
+                                                   : launch_kind<sdpa::kFP16>(D, tq, tk, tv, p, sm_count, cs);
     if (e != cudaSuccess)
         return cuda_fail(e);
     return SDPA_OK;
@@ -234,15 +249,34 @@ sdpa_status_t sdpa_fwd_fp8(const void* Q, const void* K, const void* V, void* O,
                            int Skv, int D, float scale, float descale_q, float descale_k, float descale_v,
                            int causal, void* stream)
 {
-    (void)causal;
-    (void)stream;
     const Shape s{B, Hq, Hkv, Sq, Skv, D};
     sdpa_status_t st = check_common(Q, K, V, O, s, 1, 2);
     if (st != SDPA_OK)
         return st;
     if (!valid_scale(scale) || !valid_scale(descale_q) || !valid_scale(descale_k) || !valid_scale(descale_v))
         return SDPA_ERR_SCALE;
-    return SDPA_ERR_DTYPE;
+    // the folded score scale must stay a finite, positive float
+    const double score_scale = static_cast<double>(scale) * descale_q * descale_k;
+    if (!(score_scale > 0.0) || !std::isfinite(static_cast<float>(score_scale * 1.4426950408889634)) ||
+        static_cast<float>(score_scale * 1.4426950408889634) == 0.f)
+        return SDPA_ERR_SCALE;
+
+    int dev = 0, sm_count = 0;
+    st = device_ready(&dev, &sm_count);
+    if (st != SDPA_OK)
+        return st;
+
+    CUtensorMap tq, tk, tv;
+    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (!make_map(&tq, Q, dt, 1, D, Hq, Sq, B) || !make_map(&tk, K, dt, 1, D, Hkv, Skv, B) ||
+        !make_map(&tv, V, dt, 1, D, Hkv, Skv, B))
+        return cuda_fail(cudaErrorInvalidValue);
+
+    const sdpa::Params p = make_params(O, s, score_scale, descale_v, causal);
+    const cudaError_t e = launch_kind<sdpa::kE4M3>(D, tq, tk, tv, p, sm_count, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    return SDPA_OK;
 }
 
 const char* sdpa_status_string(sdpa_status_t status)

@@ -57,6 +57,10 @@ constexpr uint32_t kRegsSoftmax = 192;
 static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * 168, "register split exceeds the launch budget");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per barrier wait
 constexpr float kRescaleThreshold = 8.0f;          // log2 units: rescale O when m grows by > 2^8
+// E4M3 P: rescale when m grows by > 2^3 and store P * 56, so that
+// P * 56 <= 2^3 * 56 = 448, the largest finite E4M3 value.
+constexpr float kRescaleThresholdFP8 = 3.0f;
+constexpr float kLog2P8Scale = 5.807354922057604f;  // log2(56)
 
 // Device error word: 0 = no error; otherwise the first failure recorded by any
 // CTA (see the codes below).  Read and cleared by the host through the C-ABI.
@@ -76,22 +80,39 @@ struct Params {
     int n_pairs;                     // ceil(Sq / 256)
     int n_ktiles;                    // ceil(Skv / 128)
     int causal;
-    float scale_log2;                // scale * log2(e): scores enter exp2
+    float scale_log2;                // scale * log2(e) (* descale_q * descale_k for E4M3)
+    float out_scale;                 // descale_v for E4M3, else 1
 };
 
-template <int D>
+// Element kinds of Q, K and V.
+enum Kind : int { kBF16 = 0, kFP16 = 1, kE4M3 = 2 };
+
+// Shared-memory and TMEM layout for head dimension D and element kind KIND.
+// A Q / K / V tile is 128 rows of D elements; TMA writes it as column blocks
+// ("chunks") of kSwz bytes per row with the matching hardware swizzle
+// (128-byte, or 64-byte when a row holds only 64 bytes).
+template <int D, int KIND>
 struct Layout {
-    static constexpr int kChunks = D / 64;                   // 128-byte swizzle column blocks
-    static constexpr int kChunkBytes = kBlockM * 128;         // 128 rows x 128 B
-    static constexpr int kTileBytes = kBlockM * D * 2;        // one Q, K or V tile
-    static constexpr int kStagesK = (D == 128) ? 3 : 4;
-    static constexpr int kStagesV = (D == 128) ? 2 : 4;
-    static constexpr int kOffQ = 0;                           // Q tile 0, Q tile 1
+    static constexpr int kEsize = (KIND == kE4M3) ? 1 : 2;
+    static constexpr int kRowBytes = D * kEsize;
+    static constexpr int kSwz = kRowBytes < 128 ? kRowBytes : 128;     // swizzle span in bytes
+    static constexpr int kChunks = kRowBytes / kSwz;
+    static constexpr int kChunkBytes = kBlockM * kSwz;
+    static constexpr int kTileBytes = kBlockM * kRowBytes;              // one Q, K or V tile
+    static constexpr int kSbo = 8 * kSwz;                              // 8-row group stride
+    static constexpr uint32_t kSwzCode = (kSwz == 128) ? 2u : 4u;        // descriptor swizzle field
+    static constexpr int kSSteps = kRowBytes / 32;                     // S MMAs: 32 bytes of K each
+    static constexpr int kKeysPerStep = 32 / kEsize;                   // P V MMAs: 16 (16-bit) or 32 (8-bit) keys
+    static constexpr int kPVSteps = kBlockN / kKeysPerStep;
+    static constexpr int kStagesK = (kTileBytes >= 32768) ? 3 : 4;
+    static constexpr int kStagesV = (kTileBytes >= 32768) ? 2 : 4;
+    static constexpr int kOffQ = 0;                                    // Q tile 0, Q tile 1
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
     static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
     static constexpr int kBarBytes = 1024;
-    static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + alignment slack
+    static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;     // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
     // TMEM columns
     __host__ __device__ static constexpr uint32_t tmem_s(int t) { return 128u * t; }        // S_t / P_t
     __host__ __device__ static constexpr uint32_t tmem_o(int t) { return 256u + 128u * t; } // O_t
@@ -145,10 +166,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
     }
 }
 
-template <bool kBF16>
+// Two floats -> two 16-bit values (round to nearest even), lo in the low half.
+template <bool kToBF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 {
-    if constexpr (kBF16) {
+    if constexpr (kToBF16) {
         __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&h);
     } else {
@@ -199,12 +221,14 @@ __device__ __forceinline__ int unit_of_round(const Params& p, int r)
     return u < p.n_units ? u : -1;
 }
 
-template <int D, bool kBF16>
+template <int D, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const Params p)
 {
-    using L = Layout<D>;
+    using L = Layout<D, KIND>;
+    constexpr bool kFP8 = (KIND == kE4M3);
+    constexpr bool kOutBF16 = (KIND != kFP16);         // E4M3 inputs give a bf16 output
     constexpr int NK = L::kStagesK;
     constexpr int NV = L::kStagesV;
     extern __shared__ uint8_t smem_raw[];
@@ -268,7 +292,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive_expect_tx(smem_u32(&bars->q_full[t]), L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_4d(sQ + t * L::kTileBytes + c * L::kChunkBytes, &tm_q, smem_u32(&bars->q_full[t]),
-                                c * 64, w.hq, w.pair * kUnitRows + t * kBlockM, w.b);
+                                c * (L::kSwz / L::kEsize), w.hq, w.pair * kUnitRows + t * kBlockM, w.b);
                 ++nq[t];
                 return true;
             };
@@ -279,7 +303,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive_expect_tx(smem_u32(&bars->k_full[s]), L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_4d(sK + s * L::kTileBytes + c * L::kChunkBytes, &tm_k, smem_u32(&bars->k_full[s]),
-                                c * 64, w.hkv, j * kBlockN, w.b);
+                                c * (L::kSwz / L::kEsize), w.hkv, j * kBlockN, w.b);
                 ++nk;
                 return true;
             };
@@ -290,7 +314,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive_expect_tx(smem_u32(&bars->v_full[s]), L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_4d(sV + s * L::kTileBytes + c * L::kChunkBytes, &tm_v, smem_u32(&bars->v_full[s]),
-                                c * 64, w.hkv, j * kBlockN, w.b);
+                                c * (L::kSwz / L::kEsize), w.hkv, j * kBlockN, w.b);
                 ++nv;
                 return true;
             };
@@ -320,42 +344,55 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       } else if (warp == kMmaWarp) {
         // ============================ MMA issuer ============================
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_f16(kBF16, kBlockM, kBlockN, false);
-            constexpr uint32_t idesc_o = idesc_f16(kBF16, kBlockM, D, true);
+            constexpr uint32_t kFmt = (KIND == kBF16) ? 1u : 0u;      // bf16 / f16 / E4M3
+            constexpr uint32_t idesc_s = idesc_make(kFmt, kBlockM, kBlockN, false);
+            constexpr uint32_t idesc_o = idesc_make(kFmt, kBlockM, D, true);
             uint32_t ck = 0, cv = 0;             // K / V tiles consumed (ring position)
             uint32_t cs[2] = {0, 0};             // S tiles issued per Q slot
             uint32_t units = 0;
             bool ok = true;
 
             // S_t = Q_t K^T for the K tile at ring position `kpos`.  Q and K
-            // tiles are K-major, 128-byte swizzled: a 16-element K step moves
-            // 32 bytes inside a 64-column block, blocks are kChunkBytes apart,
-            // 8-row groups 1024 bytes apart.
+            // tiles are K-major and swizzled: one MMA takes 32 bytes of the
+            // row (16 bf16/fp16 or 32 E4M3 elements), which moves 32 bytes
+            // inside a swizzle chunk; chunks are kChunkBytes apart and 8-row
+            // groups kSbo apart.
             auto issue_s = [&](int t, uint32_t kpos) {
                 const uint32_t d_tmem = tmem + L::tmem_s(t);
                 const uint32_t qbase = sQ + t * L::kTileBytes;
                 const uint32_t kbase = sK + (kpos % NK) * L::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-                    mma_f16_ss(d_tmem, smem_desc_sw128(qbase + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024),
-                               idesc_s, kk > 0);
+                for (int kk = 0; kk < L::kSSteps; ++kk) {
+                    const uint32_t off = (kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz;
+                    const uint64_t a = smem_desc(qbase + off, 16, L::kSbo, L::kSwzCode);
+                    const uint64_t b = smem_desc(kbase + off, 16, L::kSbo, L::kSwzCode);
+                    if constexpr (kFP8)
+                        mma_f8_ss(d_tmem, a, b, idesc_s, kk > 0);
+                    else
+                        mma_f16_ss(d_tmem, a, b, idesc_s, kk > 0);
                 }
                 mma_commit(smem_u32(&bars->s_full[t]));
                 ++cs[t];
             };
-            // O_t (+)= P_t V for the V tile at ring position `vpos`.  P_t is
-            // 128 x 128 16-bit in TMEM (8 columns per 16 keys); the V tile is
-            // MN-major (D contiguous), 128-byte swizzled: 16 keys = 2048 bytes,
-            // the next 64 columns of D one chunk further.
+            // O_t (+)= P_t V for the V tile at ring position `vpos`.  P_t sits
+            // in TMEM (128 lanes x 128 keys; 8 columns per MMA step of 16
+            // 16-bit or 32 8-bit keys).  The V tile is MN-major (D
+            // contiguous) and swizzled: a step of kKeysPerStep keys is
+            // kKeysPerStep rows of kSwz bytes; the next chunk of D columns is
+            // kChunkBytes further (leading byte offset).
             auto issue_pv = [&](int t, uint32_t vpos, bool accumulate) {
                 const uint32_t p_tmem = tmem + L::tmem_s(t);
                 const uint32_t vbase = sV + (vpos % NV) * L::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk)
-                    mma_f16_ts(tmem + L::tmem_o(t), p_tmem + kk * 8,
-                               smem_desc_sw128(vbase + kk * 2048, L::kChunkBytes, 1024), idesc_o,
-                               (accumulate || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < L::kPVSteps; ++kk) {
+                    const uint64_t b = smem_desc(vbase + kk * L::kKeysPerStep * L::kSwz, L::kChunkBytes, L::kSbo,
+                                                 L::kSwzCode);
+                    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+                    if constexpr (kFP8)
+                        mma_f8_ts(tmem + L::tmem_o(t), p_tmem + kk * 8, b, idesc_o, acc);
+                    else
+                        mma_f16_ts(tmem + L::tmem_o(t), p_tmem + kk * 8, b, idesc_o, acc);
+                }
             };
             auto wait_k = [&](uint32_t kpos) {
                 return wait_bar(smem_u32(&bars->k_full[kpos % NK]), (kpos / NK) & 1, abort, kErrWaitMma + 3);
@@ -488,38 +525,70 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 bool rescale = false;
                 if (j == 0) {
                     m = m_tile;
-                } else if (m_tile > m + kRescaleThreshold) {
+                } else if (m_tile > m + (kFP8 ? kRescaleThresholdFP8 : kRescaleThreshold)) {
                     alpha = ex2_approx(m - m_tile);
                     m = m_tile;
                     rescale = true;
                 }
-                // P = exp2(S*c - m): packed FMA for the argument, packed adds
-                // for the row sum
                 const uint64_t c2 = f32x2(c, c);
-                const uint64_t nm2 = f32x2(-m, -m);
-                uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
+                if constexpr (!kFP8) {
+                    // P = exp2(S*c - m) as 16-bit: packed FMA for the
+                    // argument, packed adds for the fp32 row sum
+                    const uint64_t nm2 = f32x2(-m, -m);
+                    uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int e = 64 * h + 2 * i;
+                            float x0, x1;
+                            f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2),
+                                        x0, x1);
+                            const float p0 = ex2_approx(x0);
+                            const float p1 = ex2_approx(x1);
+                            if (i & 1)
+                                acc1 = add_f32x2(acc1, f32x2(p0, p1));
+                            else
+                                acc0 = add_f32x2(acc0, f32x2(p0, p1));
+                            pk[i] = pack2<kOutBF16>(p0, p1);
+                        }
+                        tmem_st32(s_tmem + 32 * h, pk);
+                    }
+                    float sa, sb;
+                    f32x2_split(add_f32x2(acc0, acc1), sa, sb);
+                    l = l * alpha + (sa + sb);
+                } else {
+                    // P8 = E4M3(exp2(S*c - m) * 56), four keys per TMEM
+                    // column.  The row sum is taken over the E4M3 values
+                    // actually fed to the MMA (exact f16 conversions, f16x2
+                    // partial sums of 8 pairs each, then fp32), so that the
+                    // weights that multiply V are normalised by their own sum.
+                    const float bias = m - kLog2P8Scale;
+                    const uint64_t nb2 = f32x2(-bias, -bias);
                     uint32_t pk[32];
+                    uint32_t hs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int e = 64 * h + 2 * i;
-                        float x0, x1;
-                        f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2), x0, x1);
-                        const float p0 = ex2_approx(x0);
-                        const float p1 = ex2_approx(x1);
-                        if (i & 1)
-                            acc1 = add_f32x2(acc1, f32x2(p0, p1));
-                        else
-                            acc0 = add_f32x2(acc0, f32x2(p0, p1));
-                        pk[i] = pack2<kBF16>(p0, p1);
+                        const int e = 4 * i;
+                        float x0, x1, x2, x3;
+                        f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nb2), x0, x1);
+                        f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), c2, nb2), x2,
+                                    x3);
+                        const uint16_t lo = f32x2_to_e4m3x2(ex2_approx(x0), ex2_approx(x1));
+                        const uint16_t hi = f32x2_to_e4m3x2(ex2_approx(x2), ex2_approx(x3));
+                        pk[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+                        hs[i & 7] = add_f16x2(hs[i & 7], add_f16x2(e4m3x2_to_f16x2(lo), e4m3x2_to_f16x2(hi)));
                     }
-                    tmem_st32(s_tmem + 32 * h, pk);
+                    tmem_st32(s_tmem, pk);
+                    float sum = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float2 f = f16x2_to_f32x2(hs[k]);
+                        sum += f.x + f.y;
+                    }
+                    l = l * alpha + sum;
                 }
-                float sa, sb;
-                f32x2_split(add_f32x2(acc0, acc1), sa, sb);
-                const float sum0 = sa, sum1 = sb;
-                l = l * alpha + (sum0 + sum1);
                 // O_t holds the sum up to tile j-1 (its last P V completed before
                 // S_t(j) did); rescale it before P_t(j) V_j accumulates.
                 if (__any_sync(0xffffffffu, rescale)) {
@@ -555,15 +624,15 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tc_fence_before_sync();
             mbar_arrive(smem_u32(&bars->o_empty[t]));
             if (q_idx < p.Sq) {
-                const float inv_l = 1.f / l;
+                const float inv_l = p.out_scale / l;
                 uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.O) +
                                                       (((int64_t)w.b * p.Sq + q_idx) * p.Hq + w.hq) * (int64_t)(D * 2));
 #pragma unroll
                 for (int v = 0; v < D / 8; ++v)
-                    dst[v] = make_uint4(pack2<kBF16>(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
-                                        pack2<kBF16>(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l),
-                                        pack2<kBF16>(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l),
-                                        pack2<kBF16>(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l));
+                    dst[v] = make_uint4(pack2<kOutBF16>(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
+                                        pack2<kOutBF16>(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l),
+                                        pack2<kOutBF16>(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l),
+                                        pack2<kOutBF16>(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l));
             }
             ++units;
         }

@@ -144,3 +144,54 @@ def test_causal_gqa_4096_sampled():
 def test_mqa_sweep_sampled(B, S, causal):
     x = make_qkv(3 + S, B, 32, 1, S, S, 128, "bf16")
     sampled_check(x, causal, 600 if S >= 8192 else 1000, 3 + S)
+
+
+# ---- FP8 E4M3 inputs, bf16 output -------------------------------------------
+
+def run_gpu_fp8(x, causal, scale=None):
+    from scaled_dot_product_05_gb300 import sdpa_fwd_fp8
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+    dq, dk, dv = x.descales
+    o = sdpa_fwd_fp8(q, k, v, descale_q=dq, descale_k=dk, descale_v=dv, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return o
+
+
+FP8_SMALL = [
+    (1, 2, 2, 128, 128, 128),
+    (2, 4, 2, 384, 384, 128),
+    (1, 8, 1, 300, 300, 128),
+    (1, 4, 4, 200, 77, 128),
+    (1, 2, 2, 128, 128, 64),
+    (2, 4, 2, 333, 333, 64),
+]
+
+
+@pytest.mark.parametrize("shape", FP8_SMALL, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_fp8_small_full_compare(shape, causal):
+    B, Hq, Hkv, Sq, Skv, D = shape
+    x = make_qkv(zlib.crc32(repr((shape, causal, "e4m3")).encode()) % 100000, B, Hq, Hkv, Sq, Skv, D, "e4m3")
+    o = run_gpu_fp8(x, causal)
+    assert o.dtype == torch.bfloat16
+    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=causal, dtype="e4m3", descales=x.descales)
+    assert_close(to_np(o), ref, "e4m3", f"fp8 {shape} causal={causal}")
+
+
+def test_fp8_constant_v_is_returned():
+    # the E4M3 weights are normalised by their own sum: constant V comes back
+    # (up to the f16 partial sums and the bf16 output rounding)
+    x = make_qkv(91, 1, 4, 2, 256, 256, 128, "e4m3")
+    x.v = torch.full_like(x.v.view(torch.uint8), 0x3c).view(torch.float8_e4m3fn)   # 1.5
+    o = to_np(run_gpu_fp8(x, True))
+    assert np.abs(o - 1.5 * x.descales[2]).max() <= 4e-3 * 1.5 * x.descales[2] + 1e-6
+
+
+def test_fp8_causal_8192_sampled():
+    x = make_qkv(4, 2, 16, 16, 8192, 8192, 128, "e4m3")
+    B, Sq, Hq, D = x.q.shape
+    o = to_np(run_gpu_fp8(x, True)).reshape(-1, D)
+    rows = sample_rows(4, B, Sq, Hq, 2000)
+    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=True, dtype="e4m3", descales=x.descales, rows=rows)
+    assert_close(o[rows], ref, "e4m3", "fp8 causal S=8192")
