@@ -357,19 +357,31 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // row (16 bf16/fp16 or 32 E4M3 elements), which moves 32 bytes
             // inside a swizzle chunk; chunks are kChunkBytes apart and 8-row
             // groups kSbo apart.
+            // Descriptor bases: the start-address field (bits 0..13, in 16-byte
+            // units) is the only one that changes between the MMAs of a group,
+            // and the addresses used here never carry out of it, so each MMA's
+            // descriptors are a base plus a compile-time constant.
+            const uint64_t desc_q0 = smem_desc(sQ, 16, L::kSbo, L::kSwzCode);
+            const uint64_t desc_k0 = smem_desc(sK, 16, L::kSbo, L::kSwzCode);
+            const uint64_t desc_v0 = smem_desc(sV, L::kChunkBytes, L::kSbo, L::kSwzCode);
+            constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+
+            // S_t = Q_t K^T for the K tile at ring position `kpos`.  Q and K
+            // tiles are K-major and swizzled: one MMA takes 32 bytes of the
+            // row (16 bf16/fp16 or 32 E4M3 elements), which moves 32 bytes
+            // inside a swizzle chunk; chunks are kChunkBytes apart and 8-row
+            // groups kSbo apart.
             auto issue_s = [&](int t, uint32_t kpos) {
                 const uint32_t d_tmem = tmem + L::tmem_s(t);
-                const uint32_t qbase = sQ + t * L::kTileBytes;
-                const uint32_t kbase = sK + (kpos % NK) * L::kTileBytes;
+                const uint64_t qd = desc_q0 + (uint64_t)t * kTileUnits;
+                const uint64_t kd = desc_k0 + (uint64_t)(kpos % NK) * kTileUnits;
 #pragma unroll
                 for (int kk = 0; kk < L::kSSteps; ++kk) {
-                    const uint32_t off = (kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz;
-                    const uint64_t a = smem_desc(qbase + off, 16, L::kSbo, L::kSwzCode);
-                    const uint64_t b = smem_desc(kbase + off, 16, L::kSbo, L::kSwzCode);
+                    const uint64_t off = (uint64_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
                     if constexpr (kFP8)
-                        mma_f8_ss(d_tmem, a, b, idesc_s, kk > 0);
+                        mma_f8_ss(d_tmem, qd + off, kd + off, idesc_s, kk > 0);
                     else
-                        mma_f16_ss(d_tmem, a, b, idesc_s, kk > 0);
+                        mma_f16_ss(d_tmem, qd + off, kd + off, idesc_s, kk > 0);
                 }
                 mma_commit(smem_u32(&bars->s_full[t]));
                 ++cs[t];
@@ -382,16 +394,16 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // kChunkBytes further (leading byte offset).
             auto issue_pv = [&](int t, uint32_t vpos, bool accumulate) {
                 const uint32_t p_tmem = tmem + L::tmem_s(t);
-                const uint32_t vbase = sV + (vpos % NV) * L::kTileBytes;
+                const uint32_t o_tmem = tmem + L::tmem_o(t);
+                const uint64_t vd = desc_v0 + (uint64_t)(vpos % NV) * kTileUnits;
 #pragma unroll
                 for (int kk = 0; kk < L::kPVSteps; ++kk) {
-                    const uint64_t b = smem_desc(vbase + kk * L::kKeysPerStep * L::kSwz, L::kChunkBytes, L::kSbo,
-                                                 L::kSwzCode);
+                    const uint64_t off = (uint64_t)((kk * L::kKeysPerStep * L::kSwz) >> 4);
                     const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
                     if constexpr (kFP8)
-                        mma_f8_ts(tmem + L::tmem_o(t), p_tmem + kk * 8, b, idesc_o, acc);
+                        mma_f8_ts(o_tmem, p_tmem + kk * 8, vd + off, idesc_o, acc);
                     else
-                        mma_f16_ts(tmem + L::tmem_o(t), p_tmem + kk * 8, b, idesc_o, acc);
+                        mma_f16_ts(o_tmem, p_tmem + kk * 8, vd + off, idesc_o, acc);
                 }
             };
             auto wait_k = [&](uint32_t kpos) {
