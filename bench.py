@@ -152,6 +152,26 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside), "note": note}
 
 
+# ------------------------------------------------------------- multi-rank ----
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Slowest rank's value (all-reduce MAX); `device` is the tensor device the
+    process group's backend works on (cuda for NCCL, cpu for gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, world: int, ms_per_step: float) -> float:
+    """Weak scaling: every rank runs its own replica of the workload, so the
+    job processes world * flops_per_step per (slowest-rank) step time."""
+    return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------- CPU leg ----
 
 def oracle_sample(name, seconds_target=12.0, threads=0):
@@ -282,10 +302,7 @@ def run_gpu(args, rank, world, local_rank):
     t_wall1 = time.time()
     total_ms = start.elapsed_time(end)
     kern_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     err = sdpa_device_error()
     if err:
@@ -316,10 +333,7 @@ def run_gpu(args, rank, world, local_rank):
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     if sampler:
         sampler.stop()
 
@@ -327,7 +341,7 @@ def run_gpu(args, rank, world, local_rank):
         return 0
 
     flops = step_flops(name)
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops, world, ms_per_step)
     peaks, peak_src = load_peaks()
     avg_kernel_ms = statistics.mean(kern_ms)
     achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
@@ -351,7 +365,7 @@ def run_gpu(args, rank, world, local_rank):
                    "causal": causal, "flops_per_step": flops, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({step_bytes(name) / 1e6:.1f} MB per step, 2 rotating sets)"},
         "roofline": roofline,
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
+        "e2e": {"value": whole_job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
