@@ -309,30 +309,75 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError(f"device error word 0x{err:x}")
 
     # ---- end to end: pinned host inputs -> device -> kernel -> host output --
+    # Every step copies its inputs in from pinned host memory and its output
+    # back out.  Serial: copy in, kernel, copy out on one stream.  Pipelined:
+    # H2D, compute and D2H on three streams over the two device buffer sets,
+    # so step i+1's copy in and step i-1's copy out overlap step i's kernel
+    # (events keep each buffer set's reuse in order).
     e2e_steps = max(3, min(args.steps, 20))
     hq_, hk_, hv_ = (t.pin_memory() for t in (host.q, host.k, host.v))
-    q, k, v, o, ds = sets[0]
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hos = [torch.empty(sets[i][3].shape, dtype=sets[i][3].dtype).pin_memory() for i in range(2)]
     bi = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_))
-    bo = ho.numel() * ho.element_size()
+    bo = hos[0].numel() * hos[0].element_size()
 
-    def e2e_step():
+    def serial_step():
+        q, k, v, o, ds = sets[0]
         q.copy_(hq_, non_blocking=True)
         k.copy_(hk_, non_blocking=True)
         v.copy_(hv_, non_blocking=True)
-        launch(0, (q, k, v, o, ds))
-        ho.copy_(o, non_blocking=True)
+        launch(0, (q, k, v, o, host.descales))
+        hos[0].copy_(o, non_blocking=True)
 
     for _ in range(2):
-        e2e_step()
+        serial_step()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        e2e_step()
+        serial_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_serial_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    done_k = [torch.cuda.Event() for _ in range(2)]      # kernel on set i finished (inputs free)
+    done_o = [torch.cuda.Event() for _ in range(2)]      # copy-out of set i finished (output free)
+
+    def pipelined(nsteps, first, last):
+        for i in range(nsteps):
+            sidx = i & 1
+            q, k, v, o, ds = sets[sidx]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(done_k[sidx])
+                elif first is not None and i == 0:
+                    first.record(s_in)
+                q.copy_(hq_, non_blocking=True)
+                k.copy_(hk_, non_blocking=True)
+                v.copy_(hv_, non_blocking=True)
+                arrived = torch.cuda.Event()
+                arrived.record(s_in)
+            stream.wait_event(arrived)
+            if i >= 2:
+                stream.wait_event(done_o[sidx])
+            launch(sidx, (q, k, v, o, host.descales))              # descales of the copied data
+            done_k[sidx].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done_k[sidx])
+                hos[sidx].copy_(o, non_blocking=True)
+                done_o[sidx].record(s_out)
+        if last is not None:
+            last.record(s_out)
+
+    pipelined(4, None, None)
+    barrier()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pipelined(e2e_steps, p0, p1)
+    barrier()
+    e2e_ms = p0.elapsed_time(p1) / e2e_steps
+    # both buffer sets now hold results of the same host inputs
+    if not torch.equal(hos[0], hos[1]) or not torch.equal(hos[0], sets[0][3].cpu()):
+        raise RuntimeError("pipelined end-to-end outputs disagree")
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     if sampler:
         sampler.stop()
@@ -366,7 +411,10 @@ def run_gpu(args, rank, world, local_rank):
                    "l2": f"inputs larger than L2 ({step_bytes(name) / 1e6:.1f} MB per step, 2 rotating sets)"},
         "roofline": roofline,
         "e2e": {"value": whole_job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
+                "pipelined": "H2D / kernel / D2H on three streams over two device buffer sets",
+                "serial_ms_per_step": e2e_serial_ms,
+                "serial_value": whole_job_tflops(flops, world, e2e_serial_ms)},
         "gpu_launches": args.steps,
         "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
     }
