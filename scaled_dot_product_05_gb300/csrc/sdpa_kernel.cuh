@@ -14,9 +14,10 @@
 //   warps 0..3   softmax warpgroup for Q tile 0
 //   warps 4..7   softmax warpgroup for Q tile 1
 //   warp 8       TMA producer: Q tiles, then K_j / V_j into shared-memory rings
-//   warp 9       tcgen05 issuer (single thread): S_t = Q_t K_j^T into TMEM and
-//                O_t += P_t V_j with P_t read from TMEM
-//   warps 10,11  idle
+//   warps 9, 10  tcgen05 issuers: S_t = Q_t K_j^T into TMEM and O_t += P_t V_j
+//                with P_t read from TMEM.  bf16 / fp16: one thread per Q tile,
+//                taking turns; E4M3: thread 0 of warp 9 alone, warp 10 idle
+//   warp 11      idle
 // The two softmax warpgroups alternate with the tensor core: while one turns
 // S_t into P_t, the MMAs of the other tile run.  Each softmax thread owns one
 // query row: it reads its S row from TMEM, masks only the diagonal / tail
@@ -131,7 +132,8 @@ struct Barriers {
     uint64_t p_full[2];
     uint64_t o_full[2];
     uint64_t o_empty[2];
-    uint64_t drain;
+    uint64_t drain[2];               // one per MMA-issuing thread
+    uint32_t turn;                   // next MMA-issue turn (two-thread issuer)
     uint32_t tmem_base;
     int abort;
 };
@@ -221,6 +223,321 @@ __device__ __forceinline__ int unit_of_round(const Params& p, int r)
     return u < p.n_units ? u : -1;
 }
 
+// MMA issue from one thread (E4M3).  For E4M3 the MMAs take half the time of
+// the 16-bit ones, the tensor core waits on the softmax more than on the
+// issuer, and the turn hand-off of the two-thread issuer costs more than it
+// hides, so one thread issues for both Q tiles.
+template <int D, int KIND, int NK, int NV>
+__device__ __forceinline__ void mma_issue_single(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
+                                                 uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV)
+{
+    using L = Layout<D, KIND>;
+    constexpr bool kFP8 = (KIND == kE4M3);
+    constexpr uint32_t kFmt = (KIND == kBF16) ? 1u : 0u;      // bf16 / f16 / E4M3
+    constexpr uint32_t idesc_s = idesc_make(kFmt, kBlockM, kBlockN, false);
+    constexpr uint32_t idesc_o = idesc_make(kFmt, kBlockM, D, true);
+    uint32_t ck = 0, cv = 0;             // K / V tiles consumed (ring position)
+    uint32_t cs[2] = {0, 0};             // S tiles issued per Q slot
+    uint32_t units = 0;
+    bool ok = true;
+
+    // S_t = Q_t K^T for the K tile at ring position `kpos`.  Q and K
+    // tiles are K-major and swizzled: one MMA takes 32 bytes of the
+    // row (16 bf16/fp16 or 32 E4M3 elements), which moves 32 bytes
+    // inside a swizzle chunk; chunks are kChunkBytes apart and 8-row
+    // groups kSbo apart.
+    // Descriptor bases: the start-address field (bits 0..13, in 16-byte
+    // units) is the only one that changes between the MMAs of a group,
+    // and the addresses used here never carry out of it, so each MMA's
+    // descriptors are a base plus a compile-time constant.
+    const uint64_t desc_q0 = smem_desc(sQ, 16, L::kSbo, L::kSwzCode);
+    const uint64_t desc_k0 = smem_desc(sK, 16, L::kSbo, L::kSwzCode);
+    const uint64_t desc_v0 = smem_desc(sV, L::kChunkBytes, L::kSbo, L::kSwzCode);
+    constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+
+    // S_t = Q_t K^T for the K tile at ring position `kpos`.  Q and K
+    // tiles are K-major and swizzled: one MMA takes 32 bytes of the
+    // row (16 bf16/fp16 or 32 E4M3 elements), which moves 32 bytes
+    // inside a swizzle chunk; chunks are kChunkBytes apart and 8-row
+    // groups kSbo apart.
+    auto issue_s = [&](int t, uint32_t kpos) {
+        const uint32_t d_tmem = tmem + L::tmem_s(t);
+        const uint64_t qd = desc_q0 + (uint64_t)t * kTileUnits;
+        const uint64_t kd = desc_k0 + (uint64_t)(kpos % NK) * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < L::kSSteps; ++kk) {
+            const uint64_t off = (uint64_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
+            if constexpr (kFP8)
+                mma_f8_ss(d_tmem, qd + off, kd + off, idesc_s, kk > 0);
+            else
+                mma_f16_ss(d_tmem, qd + off, kd + off, idesc_s, kk > 0);
+        }
+        mma_commit(smem_u32(&bars->s_full[t]));
+        ++cs[t];
+    };
+    // O_t (+)= P_t V for the V tile at ring position `vpos`.  P_t sits
+    // in TMEM (128 lanes x 128 keys; 8 columns per MMA step of 16
+    // 16-bit or 32 8-bit keys).  The V tile is MN-major (D
+    // contiguous) and swizzled: a step of kKeysPerStep keys is
+    // kKeysPerStep rows of kSwz bytes; the next chunk of D columns is
+    // kChunkBytes further (leading byte offset).
+    auto issue_pv = [&](int t, uint32_t vpos, bool accumulate) {
+        const uint32_t p_tmem = tmem + L::tmem_s(t);
+        const uint32_t o_tmem = tmem + L::tmem_o(t);
+        const uint64_t vd = desc_v0 + (uint64_t)(vpos % NV) * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < L::kPVSteps; ++kk) {
+            const uint64_t off = (uint64_t)((kk * L::kKeysPerStep * L::kSwz) >> 4);
+            const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+            if constexpr (kFP8)
+                mma_f8_ts(o_tmem, p_tmem + kk * 8, vd + off, idesc_o, acc);
+            else
+                mma_f16_ts(o_tmem, p_tmem + kk * 8, vd + off, idesc_o, acc);
+        }
+    };
+    auto wait_k = [&](uint32_t kpos) {
+        return wait_bar(smem_u32(&bars->k_full[kpos % NK]), (kpos / NK) & 1, abort, kErrWaitMma + 3);
+    };
+
+    for (int r = 0; ok; ++r) {
+        const int u = unit_of_round(p, r);
+        if (u == -2)
+            break;
+        if (u < 0)
+            continue;
+        const Unit w = decode_unit(p, u);
+        const int n = w.n_kv[1];         // tile 1 visits at least as many key tiles as tile 0
+        // first K tile: S_0 for both Q tiles
+        ok = wait_k(ck);
+        for (int t = 0; ok && t < 2; ++t) {
+            ok = wait_bar(smem_u32(&bars->q_full[t]), units & 1, abort, kErrWaitMma + 1 + t);
+            if (!ok)
+                break;
+            tc_fence_after_sync();
+            issue_s(t, ck);
+            if (w.n_kv[t] == 1)
+                mma_commit(smem_u32(&bars->q_empty[t]));
+        }
+        if (!ok)
+            break;
+        mma_commit(smem_u32(&bars->k_empty[ck % NK]));
+        ++ck;
+        for (int j = 0; ok && j < n; ++j) {
+            // V_j is used by both Q tiles (tile 0 only while j < n0)
+            ok = wait_bar(smem_u32(&bars->v_full[cv % NV]), (cv / NV) & 1, abort, kErrWaitMma + 5);
+            if (!ok)
+                break;
+            const bool more = j + 1 < n;
+            bool k_ready = false;            // K_{j+1} waited for
+            for (int t = 0; t < 2; ++t) {
+                if (j >= w.n_kv[t])
+                    continue;
+                ok = wait_bar(smem_u32(&bars->p_full[t]), (cs[t] - 1) & 1, abort, kErrWaitMma + 6 + t);
+                if (ok && j == 0 && units > 0)
+                    ok = wait_bar(smem_u32(&bars->o_empty[t]), (units - 1) & 1, abort, kErrWaitMma + 8 + t);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                issue_pv(t, cv, j > 0);
+                if (j == w.n_kv[t] - 1)
+                    mma_commit(smem_u32(&bars->o_full[t]));
+                // next S_t over the same TMEM columns: ordered after this P V
+                if (j + 1 < w.n_kv[t]) {
+                    if (!k_ready && !(ok = k_ready = wait_k(ck)))
+                        break;
+                    issue_s(t, ck);
+                    if (j + 2 == w.n_kv[t])
+                        mma_commit(smem_u32(&bars->q_empty[t]));
+                }
+            }
+            if (!ok)
+                break;
+            mma_commit(smem_u32(&bars->v_empty[cv % NV]));
+            ++cv;
+            if (more) {
+                mma_commit(smem_u32(&bars->k_empty[ck % NK]));
+                ++ck;
+            }
+        }
+        ++units;
+    }
+    // every MMA this thread issued completes before TMEM is released
+    mma_commit(smem_u32(&bars->drain[0]));
+    drain_wait(smem_u32(&bars->drain[0]), 0);
+}
+
+// Shared-memory descriptor from its two 32-bit halves.  The high half (SBO,
+// version, swizzle) is the same for every operand of a kind; the low half
+// holds the start address and LBO, so each MMA's descriptor is one 32-bit add
+// away from a per-tile base.
+__device__ __forceinline__ uint64_t desc_join(uint32_t hi, uint32_t lo)
+{
+    return ((uint64_t)hi << 32) | (uint64_t)lo;
+}
+
+// MMA issue with two threads taking turns (bf16 / fp16).
+//
+// Thread 0 of warp 9 issues every MMA of Q tile 0, thread 0 of warp 10 every
+// MMA of Q tile 1.  They take strict turns through a counter in shared
+// memory, so the tensor core sees the same group order as from a single
+// issuer -- S_0(0), S_1(0), then per key tile j: [P_0 V_j, S_0(j+1)],
+// [P_1 V_j, S_1(j+1)] -- while each thread waits for its own next inputs
+// (V_j, P_t, K_{j+1}) during the other's turn, which takes that bookkeeping
+// off the tensor core's critical path.  A thread hands the turn over right
+// after issuing and commits afterwards.  Within a tile, MMAs from the one
+// issuing thread execute in issue order, so P_t V_j reads P_t before
+// S_t(j+1) overwrites those TMEM columns; the turn order itself matters for
+// speed only.  Each K / V slot is released by both threads (barrier count 2).
+template <int D, int KIND, int NK, int NV>
+__device__ __forceinline__ void mma_issue_pair(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
+                                               uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV, int t)
+{
+    using L = Layout<D, KIND>;
+    constexpr uint32_t kFmt = (KIND == kBF16) ? 1u : 0u;          // bf16 / f16
+    constexpr uint32_t idesc_s = idesc_make(kFmt, kBlockM, kBlockN, false);
+    constexpr uint32_t idesc_o = idesc_make(kFmt, kBlockM, D, true);
+    constexpr uint32_t kTileUnits = L::kTileBytes >> 4;
+    const uint32_t s_tmem = tmem + L::tmem_s(t);
+    const uint32_t o_tmem = tmem + L::tmem_o(t);
+    uint32_t ck = 0, cv = 0;             // K / V ring positions
+    uint32_t cs = 0;                     // S tiles issued for this Q tile
+    uint32_t seq = 0;                    // index of this thread's next turn in the CTA's sequence
+    uint32_t units = 0;
+    bool ok = true;
+
+    // Descriptors as (hi, lo) halves; the start address in lo moves by
+    // 16-byte units and never carries out of its 14-bit field.
+    const uint32_t desc_hi = (uint32_t)(smem_desc(0, 16, L::kSbo, L::kSwzCode) >> 32);
+    const uint32_t q_lo = ((sQ + t * L::kTileBytes) >> 4) | (1u << 16);
+    const uint32_t k_lo0 = (sK >> 4) | (1u << 16);
+    const uint32_t v_lo0 = (sV >> 4) | ((uint32_t)(L::kChunkBytes >> 4) << 16);
+
+    // S_t = Q_t K^T for the K tile at ring position `kpos` (operand layout as
+    // in the single-thread issuer).
+    auto issue_s = [&](uint32_t kpos) {
+        const uint32_t k_lo = k_lo0 + (kpos % NK) * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < L::kSSteps; ++kk) {
+            const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
+            mma_f16_ss(s_tmem, desc_join(desc_hi, q_lo + off), desc_join(desc_hi, k_lo + off), idesc_s, kk > 0);
+        }
+        ++cs;
+    };
+    // O_t (+)= P_t V for the V tile at ring position `vpos`.
+    auto issue_pv = [&](uint32_t vpos, bool accumulate) {
+        const uint32_t v_lo = v_lo0 + (vpos % NV) * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < L::kPVSteps; ++kk) {
+            const uint32_t off = (uint32_t)((kk * L::kKeysPerStep * L::kSwz) >> 4);
+            const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+            mma_f16_ts(o_tmem, s_tmem + kk * 8, desc_join(desc_hi, v_lo + off), idesc_o, acc);
+        }
+    };
+    auto wait_k = [&](uint32_t kpos) {
+        return wait_bar(smem_u32(&bars->k_full[kpos % NK]), (kpos / NK) & 1, abort, kErrWaitMma + 3);
+    };
+    auto wait_v = [&](uint32_t vpos) {
+        return wait_bar(smem_u32(&bars->v_full[vpos % NV]), (vpos / NV) & 1, abort, kErrWaitMma + 5);
+    };
+    // Wait until turn `want` comes up (bounded, like every wait here).
+    volatile uint32_t* turn = &bars->turn;
+    auto wait_turn = [&](uint32_t want) -> bool {
+        if (*turn == want)
+            return true;
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+            if (*turn == want)
+                return true;
+            if (*abort)
+                return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                atomicCAS(&g_sdpa_error, 0u, kErrWaitMma + 10 + t);
+                return false;
+            }
+        }
+    };
+
+    for (int r = 0; ok; ++r) {
+        const int u = unit_of_round(p, r);
+        if (u == -2)
+            break;
+        if (u < 0)
+            continue;
+        const Unit w = decode_unit(p, u);
+        const int n = w.n_kv[1];         // K/V tiles loaded for the unit (tile 1 sees the most)
+        const int nt = w.n_kv[t];        // of which this Q tile uses the first nt
+        // the unit's first two turns: S_0(0), S_1(0)
+        ok = wait_k(ck) && wait_bar(smem_u32(&bars->q_full[t]), units & 1, abort, kErrWaitMma + 1 + t);
+        seq += t;
+        ok = ok && wait_turn(seq);
+        if (!ok)
+            break;
+        tc_fence_after_sync();
+        issue_s(ck);
+        *turn = seq + 1;
+        seq += 2 - t;
+        mma_commit(smem_u32(&bars->s_full[t]));
+        if (nt == 1)
+            mma_commit(smem_u32(&bars->q_empty[t]));
+        mma_commit(smem_u32(&bars->k_empty[ck % NK]));
+        ++ck;
+        for (int j = 0; ok && j < n; ++j) {
+            const bool tile0_turn = j < w.n_kv[0];          // tile 0 has a turn for this j
+            const bool next_s = j + 1 < nt;
+            if (j < nt) {
+                // inputs first (during the other thread's turn), then our turn
+                ok = wait_v(cv) && wait_bar(smem_u32(&bars->p_full[t]), (cs - 1) & 1, abort, kErrWaitMma + 6 + t);
+                if (ok && j == 0 && units > 0)
+                    ok = wait_bar(smem_u32(&bars->o_empty[t]), (units - 1) & 1, abort, kErrWaitMma + 8 + t);
+                if (ok && next_s)
+                    ok = wait_k(ck);
+                if (t == 1 && tile0_turn)
+                    ++seq;                                   // tile 0's turn comes first
+                ok = ok && wait_turn(seq);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                issue_pv(cv, j > 0);
+                if (next_s)
+                    issue_s(ck);                             // ordered after this P V
+                *turn = seq + 1;                             // hand over first, then commit
+                seq += (t == 0) ? 2 : 1;                     // past tile 1's turn too
+                if (next_s)
+                    mma_commit(smem_u32(&bars->s_full[t]));
+                mma_commit(smem_u32(&bars->v_empty[cv % NV]));
+                if (j == nt - 1)
+                    mma_commit(smem_u32(&bars->o_full[t]));
+                if (next_s) {
+                    if (j + 2 == nt)
+                        mma_commit(smem_u32(&bars->q_empty[t]));
+                    mma_commit(smem_u32(&bars->k_empty[ck % NK]));
+                }
+            } else {
+                // tile 0 past its last key tile (causal): no turn; release V_j
+                // (and K_{j+1} below) once they have landed
+                if (!(ok = wait_v(cv)))
+                    break;
+                mbar_arrive(smem_u32(&bars->v_empty[cv % NV]));
+                seq += 1;                                    // tile 1's turn
+            }
+            ++cv;
+            if (j + 1 < n) {
+                if (!next_s) {
+                    if (!(ok = wait_k(ck)))
+                        break;
+                    mbar_arrive(smem_u32(&bars->k_empty[ck % NK]));
+                }
+                ++ck;
+            }
+        }
+        ++units;
+    }
+    // every MMA this thread issued completes before TMEM is released
+    mma_commit(smem_u32(&bars->drain[t]));
+    drain_wait(smem_u32(&bars->drain[t]), 0);
+}
+
 template <int D, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -231,6 +548,8 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     constexpr bool kOutBF16 = (KIND != kFP16);         // E4M3 inputs give a bf16 output
     constexpr int NK = L::kStagesK;
     constexpr int NV = L::kStagesV;
+    constexpr bool kPairIssue = !kFP8;                 // two MMA-issuing threads for bf16 / fp16
+    constexpr uint32_t kIssuers = kPairIssue ? 2u : 1u;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     auto* bars = reinterpret_cast<Barriers<NK, NV>*>(smem + L::kOffBar);
@@ -254,13 +573,15 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         for (int s = 0; s < NK; ++s) {
             mbar_init(smem_u32(&bars->k_full[s]), 1);
-            mbar_init(smem_u32(&bars->k_empty[s]), 1);
+            mbar_init(smem_u32(&bars->k_empty[s]), kIssuers);   // released by every issuing thread
         }
         for (int s = 0; s < NV; ++s) {
             mbar_init(smem_u32(&bars->v_full[s]), 1);
-            mbar_init(smem_u32(&bars->v_empty[s]), 1);
+            mbar_init(smem_u32(&bars->v_empty[s]), kIssuers);
         }
-        mbar_init(smem_u32(&bars->drain), 1);
+        mbar_init(smem_u32(&bars->drain[0]), 1);
+        mbar_init(smem_u32(&bars->drain[1]), 1);
+        bars->turn = 0;
         bars->abort = 0;
         fence_mbar_init();
     }
@@ -341,140 +662,13 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     drain_wait(smem_u32(&bars->v_full[i % NV]), (i / NV) & 1);
             }
         }
-      } else if (warp == kMmaWarp) {
-        // ============================ MMA issuer ============================
+      } else if (warp == kMmaWarp || (kPairIssue && warp == kMmaWarp + 1)) {
+        // ========================== MMA issuer(s) ===========================
         if (lane == 0) {
-            constexpr uint32_t kFmt = (KIND == kBF16) ? 1u : 0u;      // bf16 / f16 / E4M3
-            constexpr uint32_t idesc_s = idesc_make(kFmt, kBlockM, kBlockN, false);
-            constexpr uint32_t idesc_o = idesc_make(kFmt, kBlockM, D, true);
-            uint32_t ck = 0, cv = 0;             // K / V tiles consumed (ring position)
-            uint32_t cs[2] = {0, 0};             // S tiles issued per Q slot
-            uint32_t units = 0;
-            bool ok = true;
-
-            // S_t = Q_t K^T for the K tile at ring position `kpos`.  Q and K
-            // tiles are K-major and swizzled: one MMA takes 32 bytes of the
-            // row (16 bf16/fp16 or 32 E4M3 elements), which moves 32 bytes
-            // inside a swizzle chunk; chunks are kChunkBytes apart and 8-row
-            // groups kSbo apart.
-            // Descriptor bases: the start-address field (bits 0..13, in 16-byte
-            // units) is the only one that changes between the MMAs of a group,
-            // and the addresses used here never carry out of it, so each MMA's
-            // descriptors are a base plus a compile-time constant.
-            const uint64_t desc_q0 = smem_desc(sQ, 16, L::kSbo, L::kSwzCode);
-            const uint64_t desc_k0 = smem_desc(sK, 16, L::kSbo, L::kSwzCode);
-            const uint64_t desc_v0 = smem_desc(sV, L::kChunkBytes, L::kSbo, L::kSwzCode);
-            constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
-
-            // S_t = Q_t K^T for the K tile at ring position `kpos`.  Q and K
-            // tiles are K-major and swizzled: one MMA takes 32 bytes of the
-            // row (16 bf16/fp16 or 32 E4M3 elements), which moves 32 bytes
-            // inside a swizzle chunk; chunks are kChunkBytes apart and 8-row
-            // groups kSbo apart.
-            auto issue_s = [&](int t, uint32_t kpos) {
-                const uint32_t d_tmem = tmem + L::tmem_s(t);
-                const uint64_t qd = desc_q0 + (uint64_t)t * kTileUnits;
-                const uint64_t kd = desc_k0 + (uint64_t)(kpos % NK) * kTileUnits;
-#pragma unroll
-                for (int kk = 0; kk < L::kSSteps; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
-                    if constexpr (kFP8)
-                        mma_f8_ss(d_tmem, qd + off, kd + off, idesc_s, kk > 0);
-                    else
-                        mma_f16_ss(d_tmem, qd + off, kd + off, idesc_s, kk > 0);
-                }
-                mma_commit(smem_u32(&bars->s_full[t]));
-                ++cs[t];
-            };
-            // O_t (+)= P_t V for the V tile at ring position `vpos`.  P_t sits
-            // in TMEM (128 lanes x 128 keys; 8 columns per MMA step of 16
-            // 16-bit or 32 8-bit keys).  The V tile is MN-major (D
-            // contiguous) and swizzled: a step of kKeysPerStep keys is
-            // kKeysPerStep rows of kSwz bytes; the next chunk of D columns is
-            // kChunkBytes further (leading byte offset).
-            auto issue_pv = [&](int t, uint32_t vpos, bool accumulate) {
-                const uint32_t p_tmem = tmem + L::tmem_s(t);
-                const uint32_t o_tmem = tmem + L::tmem_o(t);
-                const uint64_t vd = desc_v0 + (uint64_t)(vpos % NV) * kTileUnits;
-#pragma unroll
-                for (int kk = 0; kk < L::kPVSteps; ++kk) {
-                    const uint64_t off = (uint64_t)((kk * L::kKeysPerStep * L::kSwz) >> 4);
-                    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
-                    if constexpr (kFP8)
-                        mma_f8_ts(o_tmem, p_tmem + kk * 8, vd + off, idesc_o, acc);
-                    else
-                        mma_f16_ts(o_tmem, p_tmem + kk * 8, vd + off, idesc_o, acc);
-                }
-            };
-            auto wait_k = [&](uint32_t kpos) {
-                return wait_bar(smem_u32(&bars->k_full[kpos % NK]), (kpos / NK) & 1, abort, kErrWaitMma + 3);
-            };
-
-            for (int r = 0; ok; ++r) {
-                const int u = unit_of_round(p, r);
-                if (u == -2)
-                    break;
-                if (u < 0)
-                    continue;
-                const Unit w = decode_unit(p, u);
-                const int n = w.n_kv[1];         // tile 1 visits at least as many key tiles as tile 0
-                // first K tile: S_0 for both Q tiles
-                ok = wait_k(ck);
-                for (int t = 0; ok && t < 2; ++t) {
-                    ok = wait_bar(smem_u32(&bars->q_full[t]), units & 1, abort, kErrWaitMma + 1 + t);
-                    if (!ok)
-                        break;
-                    tc_fence_after_sync();
-                    issue_s(t, ck);
-                    if (w.n_kv[t] == 1)
-                        mma_commit(smem_u32(&bars->q_empty[t]));
-                }
-                if (!ok)
-                    break;
-                mma_commit(smem_u32(&bars->k_empty[ck % NK]));
-                ++ck;
-                for (int j = 0; ok && j < n; ++j) {
-                    // V_j is used by both Q tiles (tile 0 only while j < n0)
-                    ok = wait_bar(smem_u32(&bars->v_full[cv % NV]), (cv / NV) & 1, abort, kErrWaitMma + 5);
-                    if (!ok)
-                        break;
-                    const bool more = j + 1 < n;
-                    bool k_ready = false;            // K_{j+1} waited for
-                    for (int t = 0; t < 2; ++t) {
-                        if (j >= w.n_kv[t])
-                            continue;
-                        ok = wait_bar(smem_u32(&bars->p_full[t]), (cs[t] - 1) & 1, abort, kErrWaitMma + 6 + t);
-                        if (ok && j == 0 && units > 0)
-                            ok = wait_bar(smem_u32(&bars->o_empty[t]), (units - 1) & 1, abort, kErrWaitMma + 8 + t);
-                        if (!ok)
-                            break;
-                        tc_fence_after_sync();
-                        issue_pv(t, cv, j > 0);
-                        if (j == w.n_kv[t] - 1)
-                            mma_commit(smem_u32(&bars->o_full[t]));
-                        // next S_t over the same TMEM columns: ordered after this P V
-                        if (j + 1 < w.n_kv[t]) {
-                            if (!k_ready && !(ok = k_ready = wait_k(ck)))
-                                break;
-                            issue_s(t, ck);
-                            if (j + 2 == w.n_kv[t])
-                                mma_commit(smem_u32(&bars->q_empty[t]));
-                        }
-                    }
-                    if (!ok)
-                        break;
-                    mma_commit(smem_u32(&bars->v_empty[cv % NV]));
-                    ++cv;
-                    if (more) {
-                        mma_commit(smem_u32(&bars->k_empty[ck % NK]));
-                        ++ck;
-                    }
-                }
-                ++units;
-            }
-            // every MMA this thread issued completes before TMEM is released
-            mma_commit(smem_u32(&bars->drain));
-            drain_wait(smem_u32(&bars->drain), 0);
+            if constexpr (kPairIssue)
+                mma_issue_pair<D, KIND, NK, NV>(p, bars, abort, tmem, sQ, sK, sV, warp - kMmaWarp);
+            else
+                mma_issue_single<D, KIND, NK, NV>(p, bars, abort, tmem, sQ, sK, sV);
         }
       }
     } else {
