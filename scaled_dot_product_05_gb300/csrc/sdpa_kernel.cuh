@@ -14,18 +14,24 @@
 //   warps 0..3   softmax warpgroup for Q tile 0
 //   warps 4..7   softmax warpgroup for Q tile 1
 //   warp 8       TMA producer: Q tiles, then K_j / V_j into shared-memory rings
-//   warps 9, 10  tcgen05 issuers: S_t = Q_t K_j^T into TMEM and O_t += P_t V_j
-//                with P_t read from TMEM.  bf16 / fp16: one thread per Q tile,
-//                taking turns; E4M3: thread 0 of warp 9 alone, warp 10 idle
+//   warps 9, 10  tcgen05 issuers, one thread per Q tile: S_t = Q_t K_j^T into
+//                TMEM and O_t += P_t V_j
 //   warp 11      idle
-// The two softmax warpgroups alternate with the tensor core: while one turns
-// S_t into P_t, the MMAs of the other tile run.  Each softmax thread owns one
-// query row: it reads its S row from TMEM, masks only the diagonal / tail
-// tile, keeps the running max m (exp2 domain) and sum l in fp32, writes
-// P = exp2(S*c - m) as 16-bit values over its S row, and rescales its O row in
-// TMEM only when m grows by more than 8 (a factor 256; P and l stay exact
-// relative to the m actually used).  After the unit's last tile it reads O_t,
-// releases the accumulator for the next unit, and stores O / l to HBM.
+// bf16 / fp16: P_t is written as 16-bit values over S_t's TMEM columns and
+// read from there by the P V MMA.  The two softmax warpgroups alternate with
+// the tensor core: while one turns S_t into P_t, the MMAs of the other tile
+// run; the two issuing threads take strict turns.
+// E4M3: P_t goes to shared memory, so the next S needs only that the previous
+// one has been read; both tiles take turns in one S region and each softmax
+// warpgroup runs from key tile to key tile without waiting for its P V.  The
+// row sum l_t is summed by the tensor core (P_t times a tile of ones).
+// Each softmax thread owns one query row: it reads its S row from TMEM, masks
+// only the diagonal / tail tile, keeps the running max m (exp2 domain) and
+// the sum l in fp32, forms P = exp2(S*c - m), and rescales its O row (and l)
+// only when m grows by more than 8 (a factor 256; 3 for E4M3; P and l stay
+// exact relative to the m actually used).  After the unit's last tile it
+// reads O_t, releases the accumulator for the next unit, and stores O / l to
+// HBM.
 //
 // Layout: Q, O are [B][Sq][Hq][D] and K, V are [B][Skv][Hkv][D] (section 3,
 // "Create Q, K and V test arrays": (B, T, N, H)).  Query head hq reads KV head
@@ -110,12 +116,23 @@ struct Layout {
     static constexpr int kOffQ = 0;                                    // Q tile 0, Q tile 1
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
-    static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
+    // E4M3: P_t lives in shared memory (128 rows x 128 keys, one byte each,
+    // 128-byte swizzled rows), one tile per Q tile; 16-bit P stays in TMEM.
+    // E4M3 also keeps a 16 x 128 tile of ones (E4M3 1.0 = 0x38): the MMA
+    // P_t x ones sums each row of P into TMEM.
+    static constexpr int kPTileBytes = kBlockM * kBlockN;
+    static constexpr int kOnesBytes = 16 * kBlockN;
+    static constexpr int kOffP = kOffV + kStagesV * kTileBytes;
+    static constexpr int kOffOnes = kOffP + 2 * kPTileBytes;
+    static constexpr int kOffBar = (KIND == kE4M3) ? kOffOnes + kOnesBytes : kOffP;
     static constexpr int kBarBytes = 1024;
     static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;     // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    // TMEM columns
-    __host__ __device__ static constexpr uint32_t tmem_s(int t) { return 128u * t; }        // S_t / P_t
+    // TMEM columns.  16-bit kinds: S_t / P_t at 128 t.  E4M3: both Q tiles
+    // take turns in one S region (P is in shared memory), and the freed
+    // columns hold the row sums l_t (16 columns each, all equal).
+    __host__ __device__ static constexpr uint32_t tmem_s(int t) { return (KIND == kE4M3) ? 0u : 128u * t; }
+    __host__ __device__ static constexpr uint32_t tmem_l(int t) { return 128u + 16u * t; }  // E4M3 only
     __host__ __device__ static constexpr uint32_t tmem_o(int t) { return 256u + 128u * t; } // O_t
     static constexpr uint32_t kTmemCols = 512;
 };
@@ -132,6 +149,8 @@ struct Barriers {
     uint64_t p_full[2];
     uint64_t o_full[2];
     uint64_t o_empty[2];
+    uint64_t s_free[2];              // E4M3: S_t read out of the S region (count 128)
+    uint64_t pv_done[2];             // E4M3: P_t V_j complete (P_t buffer free, O_t current)
     uint64_t drain[2];               // one per MMA-issuing thread
     uint32_t turn;                   // next MMA-issue turn (two-thread issuer)
     uint32_t tmem_base;
@@ -221,149 +240,6 @@ __device__ __forceinline__ int unit_of_round(const Params& p, int r)
         return -2;
     const int u = base + ((r & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
     return u < p.n_units ? u : -1;
-}
-
-// MMA issue from one thread (E4M3).  For E4M3 the MMAs take half the time of
-// the 16-bit ones, the tensor core waits on the softmax more than on the
-// issuer, and the turn hand-off of the two-thread issuer costs more than it
-// hides, so one thread issues for both Q tiles.
-template <int D, int KIND, int NK, int NV>
-__device__ __forceinline__ void mma_issue_single(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
-                                                 uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV)
-{
-    using L = Layout<D, KIND>;
-    constexpr bool kFP8 = (KIND == kE4M3);
-    constexpr uint32_t kFmt = (KIND == kBF16) ? 1u : 0u;      // bf16 / f16 / E4M3
-    constexpr uint32_t idesc_s = idesc_make(kFmt, kBlockM, kBlockN, false);
-    constexpr uint32_t idesc_o = idesc_make(kFmt, kBlockM, D, true);
-    uint32_t ck = 0, cv = 0;             // K / V tiles consumed (ring position)
-    uint32_t cs[2] = {0, 0};             // S tiles issued per Q slot
-    uint32_t units = 0;
-    bool ok = true;
-
-    // S_t = Q_t K^T for the K tile at ring position `kpos`.  Q and K
-    // tiles are K-major and swizzled: one MMA takes 32 bytes of the
-    // row (16 bf16/fp16 or 32 E4M3 elements), which moves 32 bytes
-    // inside a swizzle chunk; chunks are kChunkBytes apart and 8-row
-    // groups kSbo apart.
-    // Descriptor bases: the start-address field (bits 0..13, in 16-byte
-    // units) is the only one that changes between the MMAs of a group,
-    // and the addresses used here never carry out of it, so each MMA's
-    // descriptors are a base plus a compile-time constant.
-    const uint64_t desc_q0 = smem_desc(sQ, 16, L::kSbo, L::kSwzCode);
-    const uint64_t desc_k0 = smem_desc(sK, 16, L::kSbo, L::kSwzCode);
-    const uint64_t desc_v0 = smem_desc(sV, L::kChunkBytes, L::kSbo, L::kSwzCode);
-    constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
-
-    // S_t = Q_t K^T for the K tile at ring position `kpos`.  Q and K
-    // tiles are K-major and swizzled: one MMA takes 32 bytes of the
-    // row (16 bf16/fp16 or 32 E4M3 elements), which moves 32 bytes
-    // inside a swizzle chunk; chunks are kChunkBytes apart and 8-row
-    // groups kSbo apart.
-    auto issue_s = [&](int t, uint32_t kpos) {
-        const uint32_t d_tmem = tmem + L::tmem_s(t);
-        const uint64_t qd = desc_q0 + (uint64_t)t * kTileUnits;
-        const uint64_t kd = desc_k0 + (uint64_t)(kpos % NK) * kTileUnits;
-#pragma unroll
-        for (int kk = 0; kk < L::kSSteps; ++kk) {
-            const uint64_t off = (uint64_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
-            if constexpr (kFP8)
-                mma_f8_ss(d_tmem, qd + off, kd + off, idesc_s, kk > 0);
-            else
-                mma_f16_ss(d_tmem, qd + off, kd + off, idesc_s, kk > 0);
-        }
-        mma_commit(smem_u32(&bars->s_full[t]));
-        ++cs[t];
-    };
-    // O_t (+)= P_t V for the V tile at ring position `vpos`.  P_t sits
-    // in TMEM (128 lanes x 128 keys; 8 columns per MMA step of 16
-    // 16-bit or 32 8-bit keys).  The V tile is MN-major (D
-    // contiguous) and swizzled: a step of kKeysPerStep keys is
-    // kKeysPerStep rows of kSwz bytes; the next chunk of D columns is
-    // kChunkBytes further (leading byte offset).
-    auto issue_pv = [&](int t, uint32_t vpos, bool accumulate) {
-        const uint32_t p_tmem = tmem + L::tmem_s(t);
-        const uint32_t o_tmem = tmem + L::tmem_o(t);
-        const uint64_t vd = desc_v0 + (uint64_t)(vpos % NV) * kTileUnits;
-#pragma unroll
-        for (int kk = 0; kk < L::kPVSteps; ++kk) {
-            const uint64_t off = (uint64_t)((kk * L::kKeysPerStep * L::kSwz) >> 4);
-            const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
-            if constexpr (kFP8)
-                mma_f8_ts(o_tmem, p_tmem + kk * 8, vd + off, idesc_o, acc);
-            else
-                mma_f16_ts(o_tmem, p_tmem + kk * 8, vd + off, idesc_o, acc);
-        }
-    };
-    auto wait_k = [&](uint32_t kpos) {
-        return wait_bar(smem_u32(&bars->k_full[kpos % NK]), (kpos / NK) & 1, abort, kErrWaitMma + 3);
-    };
-
-    for (int r = 0; ok; ++r) {
-        const int u = unit_of_round(p, r);
-        if (u == -2)
-            break;
-        if (u < 0)
-            continue;
-        const Unit w = decode_unit(p, u);
-        const int n = w.n_kv[1];         // tile 1 visits at least as many key tiles as tile 0
-        // first K tile: S_0 for both Q tiles
-        ok = wait_k(ck);
-        for (int t = 0; ok && t < 2; ++t) {
-            ok = wait_bar(smem_u32(&bars->q_full[t]), units & 1, abort, kErrWaitMma + 1 + t);
-            if (!ok)
-                break;
-            tc_fence_after_sync();
-            issue_s(t, ck);
-            if (w.n_kv[t] == 1)
-                mma_commit(smem_u32(&bars->q_empty[t]));
-        }
-        if (!ok)
-            break;
-        mma_commit(smem_u32(&bars->k_empty[ck % NK]));
-        ++ck;
-        for (int j = 0; ok && j < n; ++j) {
-            // V_j is used by both Q tiles (tile 0 only while j < n0)
-            ok = wait_bar(smem_u32(&bars->v_full[cv % NV]), (cv / NV) & 1, abort, kErrWaitMma + 5);
-            if (!ok)
-                break;
-            const bool more = j + 1 < n;
-            bool k_ready = false;            // K_{j+1} waited for
-            for (int t = 0; t < 2; ++t) {
-                if (j >= w.n_kv[t])
-                    continue;
-                ok = wait_bar(smem_u32(&bars->p_full[t]), (cs[t] - 1) & 1, abort, kErrWaitMma + 6 + t);
-                if (ok && j == 0 && units > 0)
-                    ok = wait_bar(smem_u32(&bars->o_empty[t]), (units - 1) & 1, abort, kErrWaitMma + 8 + t);
-                if (!ok)
-                    break;
-                tc_fence_after_sync();
-                issue_pv(t, cv, j > 0);
-                if (j == w.n_kv[t] - 1)
-                    mma_commit(smem_u32(&bars->o_full[t]));
-                // next S_t over the same TMEM columns: ordered after this P V
-                if (j + 1 < w.n_kv[t]) {
-                    if (!k_ready && !(ok = k_ready = wait_k(ck)))
-                        break;
-                    issue_s(t, ck);
-                    if (j + 2 == w.n_kv[t])
-                        mma_commit(smem_u32(&bars->q_empty[t]));
-                }
-            }
-            if (!ok)
-                break;
-            mma_commit(smem_u32(&bars->v_empty[cv % NV]));
-            ++cv;
-            if (more) {
-                mma_commit(smem_u32(&bars->k_empty[ck % NK]));
-                ++ck;
-            }
-        }
-        ++units;
-    }
-    // every MMA this thread issued completes before TMEM is released
-    mma_commit(smem_u32(&bars->drain[0]));
-    drain_wait(smem_u32(&bars->drain[0]), 0);
 }
 
 // Shared-memory descriptor from its two 32-bit halves.  The high half (SBO,
@@ -538,6 +414,154 @@ __device__ __forceinline__ void mma_issue_pair(const Params& p, Barriers<NK, NV>
     drain_wait(smem_u32(&bars->drain[t]), 0);
 }
 
+// MMA issue for E4M3 with P in shared memory: one thread per Q tile (thread 0
+// of warp 9 for tile 0, of warp 10 for tile 1).
+//
+// P_t does not alias S here, so the next S needs only that the softmax has
+// read the previous one out of TMEM (s_free), not that P_t V_j has run; each
+// softmax warpgroup goes from one key tile to the next without waiting for
+// its P V.  The two Q tiles take turns in one S region, in the order
+// S_0(0), S_1(0), S_0(1), S_1(1), ... (tile 0 drops out after its last
+// causal key tile).  Each softmax warpgroup signals s_free[t] when it has
+// read its S; before each S a thread waits for the read of the S that
+// precedes it in that order, counting both tiles' S tiles so far.  That S
+// was itself issued only after its own predecessor had been read, so a
+// waiter is never two phases ahead of the barrier it waits on.  Per Q tile the issue order
+// is S_t(0), then per key tile j: S_t(j+1), P_t V_j and P_t x ones (the row
+// sum).  Both threads release every K / V slot of the unit (barrier count
+// 2), tile 0 also the causal key tile it does not visit.
+template <int D, int NK, int NV>
+__device__ __forceinline__ void mma_issue_fp8(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
+                                              uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV, uint32_t sP,
+                                              uint32_t sOnes, int t)
+{
+    using L = Layout<D, kE4M3>;
+    constexpr uint32_t idesc_s = idesc_make(0u, kBlockM, kBlockN, false);   // E4M3 x E4M3 -> f32
+    constexpr uint32_t idesc_o = idesc_make(0u, kBlockM, D, true);
+    constexpr uint32_t idesc_l = idesc_make(0u, kBlockM, 16, false);
+    constexpr uint32_t kTileUnits = L::kTileBytes >> 4;
+    const uint32_t s_tmem = tmem + L::tmem_s(t);
+    const uint32_t o_tmem = tmem + L::tmem_o(t);
+    const uint32_t l_tmem = tmem + L::tmem_l(t);
+    uint32_t ck = 0, cv = 0;             // K / V ring positions at the start of the unit
+    uint32_t sbase[2] = {0, 0};          // S tiles of Q tile 0 / 1 before this unit
+    uint32_t npv = 0;                    // P V groups issued for this Q tile
+    uint32_t units = 0;
+    bool ok = true;
+
+    // Descriptors as (hi, lo) halves (see mma_issue_pair).  P and the ones
+    // tile have 128-byte rows: one 128-byte swizzle span, 8-row groups 1024
+    // bytes apart.
+    const uint32_t desc_hi = (uint32_t)(smem_desc(0, 16, L::kSbo, L::kSwzCode) >> 32);
+    const uint32_t p_hi = (uint32_t)(smem_desc(0, 16, 1024, 2u) >> 32);
+    const uint32_t q_lo = ((sQ + t * L::kTileBytes) >> 4) | (1u << 16);
+    const uint32_t k_lo0 = (sK >> 4) | (1u << 16);
+    const uint32_t v_lo0 = (sV >> 4) | ((uint32_t)(L::kChunkBytes >> 4) << 16);
+    const uint32_t p_lo = ((sP + t * L::kPTileBytes) >> 4) | (1u << 16);
+    const uint32_t ones_lo = (sOnes >> 4) | (1u << 16);
+
+    auto wait_k = [&](uint32_t kpos) {
+        return wait_bar(smem_u32(&bars->k_full[kpos % NK]), (kpos / NK) & 1, abort, kErrWaitMma + 3);
+    };
+    auto wait_v = [&](uint32_t vpos) {
+        return wait_bar(smem_u32(&bars->v_full[vpos % NV]), (vpos / NV) & 1, abort, kErrWaitMma + 5);
+    };
+    // S_t(j) = Q_t K_j^T into the S region, once K_j has landed and the S
+    // before it in the region's sequence has been read out.
+    auto issue_s = [&](const Unit& w, int j) -> bool {
+        const uint32_t kpos = ck + j;
+        // the S before this one in the region: S_1(j-1) for tile 0, S_0(j)
+        // for tile 1 while tile 0 still has key tiles, else S_1(j-1); as a
+        // count of that tile's S tiles read so far (0: none to wait for)
+        const int pt = (t == 1 && j < w.n_kv[0]) ? 0 : 1;
+        const uint32_t need = sbase[pt] + (uint32_t)((pt == 0) ? j + 1 : j);
+        bool r = wait_k(kpos);
+        if (r && j == 0)
+            r = wait_bar(smem_u32(&bars->q_full[t]), units & 1, abort, kErrWaitMma + 1 + t);
+        if (r && need > 0)
+            r = wait_bar(smem_u32(&bars->s_free[pt]), (need - 1) & 1, abort, kErrWaitMma + 12 + t);
+        if (!r)
+            return false;
+        tc_fence_after_sync();
+        const uint32_t k_lo = k_lo0 + (kpos % NK) * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < L::kSSteps; ++kk) {
+            const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
+            mma_f8_ss(s_tmem, desc_join(desc_hi, q_lo + off), desc_join(desc_hi, k_lo + off), idesc_s, kk > 0);
+        }
+        mma_commit(smem_u32(&bars->s_full[t]));
+        if (j == w.n_kv[t] - 1)
+            mma_commit(smem_u32(&bars->q_empty[t]));
+        mma_commit(smem_u32(&bars->k_empty[kpos % NK]));
+        return true;
+    };
+    // O_t (+)= P_t V_j and l_t (+)= P_t ones: P_t (K-major, keys contiguous),
+    // V_j (MN-major) and the ones tile (K-major) from shared memory, 32 keys
+    // per MMA.
+    auto issue_pv = [&](const Unit& w, int j) -> bool {
+        const uint32_t vpos = cv + j;
+        bool r = wait_v(vpos) && wait_bar(smem_u32(&bars->p_full[t]), npv & 1, abort, kErrWaitMma + 6 + t);
+        if (r && j == 0 && units > 0)
+            r = wait_bar(smem_u32(&bars->o_empty[t]), (units - 1) & 1, abort, kErrWaitMma + 8 + t);
+        if (!r)
+            return false;
+        tc_fence_after_sync();
+        const uint32_t v_lo = v_lo0 + (vpos % NV) * kTileUnits;
+#pragma unroll
+        for (int kk = 0; kk < L::kPVSteps; ++kk) {
+            const uint32_t off_p = (uint32_t)((kk * 32) >> 4);
+            const uint32_t off_v = (uint32_t)((kk * L::kKeysPerStep * L::kSwz) >> 4);
+            mma_f8_ss(o_tmem, desc_join(p_hi, p_lo + off_p), desc_join(desc_hi, v_lo + off_v), idesc_o,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < L::kPVSteps; ++kk) {
+            const uint32_t off = (uint32_t)((kk * 32) >> 4);
+            mma_f8_ss(l_tmem, desc_join(p_hi, p_lo + off), desc_join(p_hi, ones_lo + off), idesc_l,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars->pv_done[t]));
+        mma_commit(smem_u32(&bars->v_empty[vpos % NV]));
+        if (j == w.n_kv[t] - 1)
+            mma_commit(smem_u32(&bars->o_full[t]));
+        ++npv;
+        return true;
+    };
+
+    for (int r = 0; ok; ++r) {
+        const int u = unit_of_round(p, r);
+        if (u == -2)
+            break;
+        if (u < 0)
+            continue;
+        const Unit w = decode_unit(p, u);
+        const int n = w.n_kv[1];         // K/V tiles loaded for the unit (tile 1 sees the most)
+        const int nt = w.n_kv[t];        // of which this Q tile uses the first nt
+        ok = issue_s(w, 0);
+        for (int j = 0; ok && j < nt; ++j) {
+            if (j + 1 < nt)
+                ok = issue_s(w, j + 1);
+            ok = ok && issue_pv(w, j);
+        }
+        // key tiles this Q tile does not visit (tile 0, causal): release them
+        for (int j = nt; ok && j < n; ++j) {
+            ok = wait_k(ck + j) && wait_v(cv + j);
+            if (ok) {
+                mbar_arrive(smem_u32(&bars->k_empty[(ck + j) % NK]));
+                mbar_arrive(smem_u32(&bars->v_empty[(cv + j) % NV]));
+            }
+        }
+        ck += n;
+        cv += n;
+        sbase[0] += (uint32_t)w.n_kv[0];
+        sbase[1] += (uint32_t)w.n_kv[1];
+        ++units;
+    }
+    // every MMA this thread issued completes before TMEM is released
+    mma_commit(smem_u32(&bars->drain[t]));
+    drain_wait(smem_u32(&bars->drain[t]), 0);
+}
+
 template <int D, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -548,8 +572,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     constexpr bool kOutBF16 = (KIND != kFP16);         // E4M3 inputs give a bf16 output
     constexpr int NK = L::kStagesK;
     constexpr int NV = L::kStagesV;
-    constexpr bool kPairIssue = !kFP8;                 // two MMA-issuing threads for bf16 / fp16
-    constexpr uint32_t kIssuers = kPairIssue ? 2u : 1u;
+    constexpr uint32_t kIssuers = 2;                   // MMA-issuing threads, one per Q tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     auto* bars = reinterpret_cast<Barriers<NK, NV>*>(smem + L::kOffBar);
@@ -561,6 +584,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t sQ = smem_u32(smem + L::kOffQ);
     const uint32_t sK = smem_u32(smem + L::kOffK);
     const uint32_t sV = smem_u32(smem + L::kOffV);
+    const uint32_t sP = smem_u32(smem + L::kOffP);     // E4M3 only
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
@@ -570,6 +594,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(smem_u32(&bars->p_full[t]), 128);
             mbar_init(smem_u32(&bars->o_full[t]), 1);
             mbar_init(smem_u32(&bars->o_empty[t]), 128);
+            mbar_init(smem_u32(&bars->pv_done[t]), 1);
         }
         for (int s = 0; s < NK; ++s) {
             mbar_init(smem_u32(&bars->k_full[s]), 1);
@@ -579,6 +604,8 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(smem_u32(&bars->v_full[s]), 1);
             mbar_init(smem_u32(&bars->v_empty[s]), kIssuers);
         }
+        mbar_init(smem_u32(&bars->s_free[0]), 128);
+        mbar_init(smem_u32(&bars->s_free[1]), 128);
         mbar_init(smem_u32(&bars->drain[0]), 1);
         mbar_init(smem_u32(&bars->drain[1]), 1);
         bars->turn = 0;
@@ -593,6 +620,12 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&bars->tmem_base), L::kTmemCols);
         tmem_relinquish();
+    }
+    if constexpr (kFP8) {
+        uint32_t* ones = reinterpret_cast<uint32_t*>(smem + L::kOffOnes);
+        for (int i = threadIdx.x; i < L::kOnesBytes / 4; i += kThreads)
+            ones[i] = 0x38383838u;
+        fence_proxy_async_smem();                      // read by tcgen05.mma
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -662,13 +695,14 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     drain_wait(smem_u32(&bars->v_full[i % NV]), (i / NV) & 1);
             }
         }
-      } else if (warp == kMmaWarp || (kPairIssue && warp == kMmaWarp + 1)) {
-        // ========================== MMA issuer(s) ===========================
+      } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+        // =========================== MMA issuers ============================
         if (lane == 0) {
-            if constexpr (kPairIssue)
-                mma_issue_pair<D, KIND, NK, NV>(p, bars, abort, tmem, sQ, sK, sV, warp - kMmaWarp);
+            if constexpr (kFP8)
+                mma_issue_fp8<D, NK, NV>(p, bars, abort, tmem, sQ, sK, sV, sP, smem_u32(smem + L::kOffOnes),
+                                         warp - kMmaWarp);
             else
-                mma_issue_single<D, KIND, NK, NV>(p, bars, abort, tmem, sQ, sK, sV);
+                mma_issue_pair<D, KIND, NK, NV>(p, bars, abort, tmem, sQ, sK, sV, warp - kMmaWarp);
         }
       }
     } else {
@@ -682,8 +716,23 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t o_tmem = tmem + lane_addr + L::tmem_o(t);
         const float c = p.scale_log2;
         uint32_t cs = 0;                                   // S tiles consumed
+        uint32_t np = 0;                                   // E4M3: P tiles handed to the MMA
         uint32_t units = 0;
         bool ok = true;
+        const uint32_t p_row = sP + t * L::kPTileBytes + row * 128;   // E4M3: this row of P_t
+        const uint32_t l_tmem = tmem + lane_addr + L::tmem_l(t);      // E4M3: row sum of P_t
+        // O_t *= alpha in TMEM (the running max grew past the threshold)
+        auto rescale_o = [&](float alpha) {
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                tmem_ld32_wait(o_tmem + cc * 32, o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st32(o_tmem + cc * 32, o);
+            }
+        };
         for (int r = 0; ok; ++r) {
             const int u = unit_of_round(p, r);
             if (u == -2)
@@ -697,7 +746,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (p.causal && q_idx < limit)
                 limit = q_idx;
             float m = -INFINITY;                           // running max of S*c
-            float l = 0.f;                                 // running sum of exp2(S*c - m)
+            float l = 0.f;                                 // running sum of exp2(S*c - m) (16-bit kinds)
             for (int j = 0; j < n; ++j) {
                 ok = __all_sync(0xffffffffu,
                                 wait_bar(smem_u32(&bars->s_full[t]), cs & 1, abort, kErrWaitSoftmax + 1 + t));
@@ -707,6 +756,11 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tc_fence_after_sync();
                 uint32_t r[128];
                 tmem_ld128_wait(s_tmem, s_tmem + 32, s_tmem + 64, s_tmem + 96, r);
+                if constexpr (kFP8) {
+                    // E4M3: the S region is free for the next S as soon as it is read
+                    tc_fence_before_sync();
+                    mbar_arrive(smem_u32(&bars->s_free[t]));
+                }
                 const int k0 = j * kBlockN;
                 if (k0 + kBlockN - 1 > limit) {
 #pragma unroll
@@ -764,16 +818,18 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     float sa, sb;
                     f32x2_split(add_f32x2(acc0, acc1), sa, sb);
                     l = l * alpha + (sa + sb);
+                    // O_t holds the sum up to tile j-1 (its last P V completed
+                    // before S_t(j) did); rescale it before P_t(j) V_j accumulates.
+                    if (__any_sync(0xffffffffu, rescale))
+                        rescale_o(alpha);
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    mbar_arrive(smem_u32(&bars->p_full[t]));
                 } else {
-                    // P8 = E4M3(exp2(S*c - m) * 56), four keys per TMEM
-                    // column.  The row sum is taken over the E4M3 values
-                    // actually fed to the MMA (exact f16 conversions, f16x2
-                    // partial sums of 8 pairs each, then fp32), so that the
-                    // weights that multiply V are normalised by their own sum.
+                    // P8 = E4M3(exp2(S*c - m) * 56), four keys per 32-bit word
                     const float bias = m - kLog2P8Scale;
                     const uint64_t nb2 = f32x2(-bias, -bias);
                     uint32_t pk[32];
-                    uint32_t hs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int e = 4 * i;
@@ -781,36 +837,33 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nb2), x0, x1);
                         f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), c2, nb2), x2,
                                     x3);
-                        const uint16_t lo = f32x2_to_e4m3x2(ex2_approx(x0), ex2_approx(x1));
-                        const uint16_t hi = f32x2_to_e4m3x2(ex2_approx(x2), ex2_approx(x3));
-                        pk[i] = (uint32_t)lo | ((uint32_t)hi << 16);
-                        hs[i & 7] = add_f16x2(hs[i & 7], add_f16x2(e4m3x2_to_f16x2(lo), e4m3x2_to_f16x2(hi)));
+                        const uint32_t lo = f32x2_to_e4m3x2(ex2_approx(x0), ex2_approx(x1));
+                        const uint32_t hi = f32x2_to_e4m3x2(ex2_approx(x2), ex2_approx(x3));
+                        pk[i] = lo | (hi << 16);
                     }
-                    tmem_st32(s_tmem, pk);
-                    float sum = 0.f;
+                    // the previous P_t V has read the P_t buffer and updated O_t
+                    if (np > 0)
+                        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[t]), (np - 1) & 1, abort,
+                                                              kErrWaitSoftmax + 5 + t));
+                    if (!ok)
+                        break;
+                    ++np;
+                    tc_fence_after_sync();
+                    if (__any_sync(0xffffffffu, rescale)) {
+                        rescale_o(alpha);
+                        tmem_st1(l_tmem, __float_as_uint(__uint_as_float(tmem_ld1_wait(l_tmem)) * alpha));
+                    }
+                    // this row's 128 keys: one 128-byte row of the K-major P
+                    // tile, 16-byte chunk c at position c ^ (row & 7)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float2 f = f16x2_to_f32x2(hs[k]);
-                        sum += f.x + f.y;
-                    }
-                    l = l * alpha + sum;
+                    for (int cc = 0; cc < 8; ++cc)
+                        st_shared_v4(p_row + (uint32_t)((cc ^ (row & 7)) << 4), pk[4 * cc], pk[4 * cc + 1],
+                                     pk[4 * cc + 2], pk[4 * cc + 3]);
+                    fence_proxy_async_smem();
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    mbar_arrive(smem_u32(&bars->p_full[t]));
                 }
-                // O_t holds the sum up to tile j-1 (its last P V completed before
-                // S_t(j) did); rescale it before P_t(j) V_j accumulates.
-                if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        tmem_ld32_wait(o_tmem + cc * 32, o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(o_tmem + cc * 32, o);
-                    }
-                }
-                tmem_st_wait();
-                tc_fence_before_sync();
-                mbar_arrive(smem_u32(&bars->p_full[t]));
             }
             if (!ok)
                 break;
@@ -827,6 +880,8 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld32_wait(o_tmem, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
                 tmem_ld32_wait(o_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
             }
+            if constexpr (kFP8)
+                l = __uint_as_float(tmem_ld1_wait(l_tmem));   // sum of the E4M3 P values (tensor core, fp32)
             tc_fence_before_sync();
             mbar_arrive(smem_u32(&bars->o_empty[t]));
             if (q_idx < p.Sq) {
