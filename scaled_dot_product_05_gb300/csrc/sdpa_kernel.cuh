@@ -14,17 +14,13 @@
 //   warps 0..3   softmax warpgroup for Q tile 0
 //   warps 4..7   softmax warpgroup for Q tile 1
 //   warp 8       TMA producer: Q tiles, then K_j / V_j into shared-memory rings
-//   warps 9, 10  tcgen05 issuers, one thread per Q tile: S_t = Q_t K_j^T into
-//                TMEM and O_t += P_t V_j
-//   warp 11      idle
-// bf16 / fp16: P_t is written as 16-bit values over S_t's TMEM columns and
-// read from there by the P V MMA.  The two softmax warpgroups alternate with
-// the tensor core: while one turns S_t into P_t, the MMAs of the other tile
-// run; the two issuing threads take strict turns.
-// E4M3: P_t goes to shared memory, so the next S needs only that the previous
-// one has been read; both tiles take turns in one S region and each softmax
-// warpgroup runs from key tile to key tile without waiting for its P V.  The
-// row sum l_t is summed by the tensor core (P_t times a tile of ones).
+//   warps 9, 10  tcgen05 issue of O_t += P_t V_j for Q tile 0 / 1
+//   warp 11      tcgen05 issue of every S_t = Q_t K_j^T
+// Both Q tiles take turns in one TMEM S region.  P_t never overwrites S: the
+// 16-bit P_t has its own TMEM columns, the E4M3 P_t sits in shared memory
+// (and the tensor core sums its rows, P_t times a tile of ones).  So S_t(j+1)
+// is computed while the softmax works on S_t(j), and each softmax warpgroup
+// runs from key tile to key tile without waiting for its P V.
 // Each softmax thread owns one query row: it reads its S row from TMEM, masks
 // only the diagonal / tail tile, keeps the running max m (exp2 domain) and
 // the sum l in fp32, forms P = exp2(S*c - m), and rescales its O row (and l)
@@ -55,7 +51,8 @@ constexpr int kBlockN = 128;         // keys per K/V tile
 constexpr int kUnitRows = 2 * kBlockM;
 constexpr int kThreads = 384;        // 12 warps
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;          // P V issue for Q tile 0; warp 10 for Q tile 1
+constexpr int kSMmaWarp = 11;        // S issue
 // Register split: launched at 168 per thread (384 x 168 = 64512); the
 // producer warpgroup (warps 8..11) drops to 104 and the two softmax warpgroups
 // rise to 192: 128 x 104 + 256 x 192 = 62464 <= 64512.
@@ -128,11 +125,13 @@ struct Layout {
     static constexpr int kBarBytes = 1024;
     static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;     // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    // TMEM columns.  16-bit kinds: S_t / P_t at 128 t.  E4M3: both Q tiles
-    // take turns in one S region (P is in shared memory), and the freed
-    // columns hold the row sums l_t (16 columns each, all equal).
-    __host__ __device__ static constexpr uint32_t tmem_s(int t) { return (KIND == kE4M3) ? 0u : 128u * t; }
-    __host__ __device__ static constexpr uint32_t tmem_l(int t) { return 128u + 16u * t; }  // E4M3 only
+    // TMEM columns.  Both Q tiles take turns in one S region (columns 0..127).
+    // 16-bit kinds: P_t in columns 128 + 64 t (two values per column).  E4M3:
+    // P is in shared memory and columns 128 + 16 t hold the row sums l_t (16
+    // columns each, all equal).  O_t in columns 256 + 128 t.
+    __host__ __device__ static constexpr uint32_t tmem_s(int) { return 0u; }
+    __host__ __device__ static constexpr uint32_t tmem_p(int t) { return 128u + 64u * t; }  // 16-bit kinds
+    __host__ __device__ static constexpr uint32_t tmem_l(int t) { return 128u + 16u * t; }  // E4M3
     __host__ __device__ static constexpr uint32_t tmem_o(int t) { return 256u + 128u * t; } // O_t
     static constexpr uint32_t kTmemCols = 512;
 };
@@ -149,10 +148,9 @@ struct Barriers {
     uint64_t p_full[2];
     uint64_t o_full[2];
     uint64_t o_empty[2];
-    uint64_t s_free[2];              // E4M3: S_t read out of the S region (count 128)
-    uint64_t pv_done[2];             // E4M3: P_t V_j complete (P_t buffer free, O_t current)
-    uint64_t drain[2];               // one per MMA-issuing thread
-    uint32_t turn;                   // next MMA-issue turn (two-thread issuer)
+    uint64_t s_free[2];              // S_t read out of the S region (count 128)
+    uint64_t pv_done[2];             // P_t V_j complete (P_t buffer free, O_t current)
+    uint64_t drain[3];               // one per MMA-issuing thread
     uint32_t tmem_base;
     int abort;
 };
@@ -251,89 +249,43 @@ __device__ __forceinline__ uint64_t desc_join(uint32_t hi, uint32_t lo)
     return ((uint64_t)hi << 32) | (uint64_t)lo;
 }
 
-// MMA issue with two threads taking turns (bf16 / fp16).
+// MMA issue.  P_t never aliases S (16-bit P has its own TMEM columns, E4M3 P
+// sits in shared memory), so the next S needs only that the softmax has read
+// the previous one out of TMEM, not that P_t V_j has run: S_t(j+1) is
+// computed while the softmax works on S_t(j), and each softmax warpgroup
+// goes from one key tile to the next without waiting for its P V.  Both Q
+// tiles take turns in one S region.
 //
-// Thread 0 of warp 9 issues every MMA of Q tile 0, thread 0 of warp 10 every
-// MMA of Q tile 1.  They take strict turns through a counter in shared
-// memory, so the tensor core sees the same group order as from a single
-// issuer -- S_0(0), S_1(0), then per key tile j: [P_0 V_j, S_0(j+1)],
-// [P_1 V_j, S_1(j+1)] -- while each thread waits for its own next inputs
-// (V_j, P_t, K_{j+1}) during the other's turn, which takes that bookkeeping
-// off the tensor core's critical path.  A thread hands the turn over right
-// after issuing and commits afterwards.  Within a tile, MMAs from the one
-// issuing thread execute in issue order, so P_t V_j reads P_t before
-// S_t(j+1) overwrites those TMEM columns; the turn order itself matters for
-// speed only.  Each K / V slot is released by both threads (barrier count 2).
+// Three issuing threads: thread 0 of warp 11 issues every S, in region order
+// S_0(0), S_1(0), S_0(1), S_1(1), ... (tile 0 drops out after its last causal
+// key tile); thread 0 of warp 9 / 10 issues P_t V_j for Q tile 0 / 1.  The S
+// thread waits, before each S, for the softmax of the previous S's tile to
+// have read it (s_free[t]); as it waits for every S in order, no s_free
+// barrier can be two phases away from the phase it waits for.
+
+// Descriptors as (hi, lo) halves.  Q and K tiles are K-major and swizzled:
+// one MMA takes 32 bytes of the row (16 bf16/fp16 or 32 E4M3 elements), which
+// moves 32 bytes inside a swizzle chunk; chunks are kChunkBytes apart and
+// 8-row groups kSbo apart.  The V tile is MN-major (D contiguous): a step of
+// kKeysPerStep keys is kKeysPerStep rows of kSwz bytes, the next chunk of D
+// columns kChunkBytes further (LBO).  The E4M3 P tile and the ones tile have
+// 128-byte rows: one 128-byte swizzle span, 8-row groups 1024 bytes apart.
 template <int D, int KIND, int NK, int NV>
-__device__ __forceinline__ void mma_issue_pair(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
-                                               uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV, int t)
+__device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
+                                            uint32_t tmem, uint32_t sQ, uint32_t sK)
 {
     using L = Layout<D, KIND>;
-    constexpr uint32_t kFmt = (KIND == kBF16) ? 1u : 0u;          // bf16 / f16
+    constexpr uint32_t kFmt = (KIND == kBF16) ? 1u : 0u;          // bf16 / f16 / E4M3
     constexpr uint32_t idesc_s = idesc_make(kFmt, kBlockM, kBlockN, false);
-    constexpr uint32_t idesc_o = idesc_make(kFmt, kBlockM, D, true);
     constexpr uint32_t kTileUnits = L::kTileBytes >> 4;
-    const uint32_t s_tmem = tmem + L::tmem_s(t);
-    const uint32_t o_tmem = tmem + L::tmem_o(t);
-    uint32_t ck = 0, cv = 0;             // K / V ring positions
-    uint32_t cs = 0;                     // S tiles issued for this Q tile
-    uint32_t seq = 0;                    // index of this thread's next turn in the CTA's sequence
+    const uint32_t s_tmem = tmem + L::tmem_s(0);
+    const uint32_t desc_hi = (uint32_t)(smem_desc(0, 16, L::kSbo, L::kSwzCode) >> 32);
+    const uint32_t k_lo0 = (sK >> 4) | (1u << 16);
+    uint32_t ck = 0;                     // K ring position
+    uint32_t ns[2] = {0, 0};             // S tiles issued per Q tile
+    int prev = -1;                       // Q tile of the last S issued
     uint32_t units = 0;
     bool ok = true;
-
-    // Descriptors as (hi, lo) halves; the start address in lo moves by
-    // 16-byte units and never carries out of its 14-bit field.
-    const uint32_t desc_hi = (uint32_t)(smem_desc(0, 16, L::kSbo, L::kSwzCode) >> 32);
-    const uint32_t q_lo = ((sQ + t * L::kTileBytes) >> 4) | (1u << 16);
-    const uint32_t k_lo0 = (sK >> 4) | (1u << 16);
-    const uint32_t v_lo0 = (sV >> 4) | ((uint32_t)(L::kChunkBytes >> 4) << 16);
-
-    // S_t = Q_t K^T for the K tile at ring position `kpos` (operand layout as
-    // in the single-thread issuer).
-    auto issue_s = [&](uint32_t kpos) {
-        const uint32_t k_lo = k_lo0 + (kpos % NK) * kTileUnits;
-#pragma unroll
-        for (int kk = 0; kk < L::kSSteps; ++kk) {
-            const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
-            mma_f16_ss(s_tmem, desc_join(desc_hi, q_lo + off), desc_join(desc_hi, k_lo + off), idesc_s, kk > 0);
-        }
-        ++cs;
-    };
-    // O_t (+)= P_t V for the V tile at ring position `vpos`.
-    auto issue_pv = [&](uint32_t vpos, bool accumulate) {
-        const uint32_t v_lo = v_lo0 + (vpos % NV) * kTileUnits;
-#pragma unroll
-        for (int kk = 0; kk < L::kPVSteps; ++kk) {
-            const uint32_t off = (uint32_t)((kk * L::kKeysPerStep * L::kSwz) >> 4);
-            const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
-            mma_f16_ts(o_tmem, s_tmem + kk * 8, desc_join(desc_hi, v_lo + off), idesc_o, acc);
-        }
-    };
-    auto wait_k = [&](uint32_t kpos) {
-        return wait_bar(smem_u32(&bars->k_full[kpos % NK]), (kpos / NK) & 1, abort, kErrWaitMma + 3);
-    };
-    auto wait_v = [&](uint32_t vpos) {
-        return wait_bar(smem_u32(&bars->v_full[vpos % NV]), (vpos / NV) & 1, abort, kErrWaitMma + 5);
-    };
-    // Wait until turn `want` comes up (bounded, like every wait here).
-    volatile uint32_t* turn = &bars->turn;
-    auto wait_turn = [&](uint32_t want) -> bool {
-        if (*turn == want)
-            return true;
-        const uint64_t t0 = global_timer_ns();
-        for (;;) {
-            if (*turn == want)
-                return true;
-            if (*abort)
-                return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                *abort = 1;
-                atomicCAS(&g_sdpa_error, 0u, kErrWaitMma + 10 + t);
-                return false;
-            }
-        }
-    };
-
     for (int r = 0; ok; ++r) {
         const int u = unit_of_round(p, r);
         if (u == -2)
@@ -341,193 +293,76 @@ __device__ __forceinline__ void mma_issue_pair(const Params& p, Barriers<NK, NV>
         if (u < 0)
             continue;
         const Unit w = decode_unit(p, u);
-        const int n = w.n_kv[1];         // K/V tiles loaded for the unit (tile 1 sees the most)
-        const int nt = w.n_kv[t];        // of which this Q tile uses the first nt
-        // the unit's first two turns: S_0(0), S_1(0)
-        ok = wait_k(ck) && wait_bar(smem_u32(&bars->q_full[t]), units & 1, abort, kErrWaitMma + 1 + t);
-        seq += t;
-        ok = ok && wait_turn(seq);
-        if (!ok)
-            break;
-        tc_fence_after_sync();
-        issue_s(ck);
-        *turn = seq + 1;
-        seq += 2 - t;
-        mma_commit(smem_u32(&bars->s_full[t]));
-        if (nt == 1)
-            mma_commit(smem_u32(&bars->q_empty[t]));
-        mma_commit(smem_u32(&bars->k_empty[ck % NK]));
-        ++ck;
+        const int n = w.n_kv[1];         // tile 1 visits at least as many key tiles as tile 0
         for (int j = 0; ok && j < n; ++j) {
-            const bool tile0_turn = j < w.n_kv[0];          // tile 0 has a turn for this j
-            const bool next_s = j + 1 < nt;
-            if (j < nt) {
-                // inputs first (during the other thread's turn), then our turn
-                ok = wait_v(cv) && wait_bar(smem_u32(&bars->p_full[t]), (cs - 1) & 1, abort, kErrWaitMma + 6 + t);
-                if (ok && j == 0 && units > 0)
-                    ok = wait_bar(smem_u32(&bars->o_empty[t]), (units - 1) & 1, abort, kErrWaitMma + 8 + t);
-                if (ok && next_s)
-                    ok = wait_k(ck);
-                if (t == 1 && tile0_turn)
-                    ++seq;                                   // tile 0's turn comes first
-                ok = ok && wait_turn(seq);
+            ok = wait_bar(smem_u32(&bars->k_full[ck % NK]), (ck / NK) & 1, abort, kErrWaitMma + 3);
+            for (int t = 0; ok && t < 2; ++t) {
+                if (j >= w.n_kv[t])
+                    continue;
+                if (j == 0)
+                    ok = wait_bar(smem_u32(&bars->q_full[t]), units & 1, abort, kErrWaitMma + 1 + t);
+                if (ok && prev >= 0)         // the previous S has been read out of the region
+                    ok = wait_bar(smem_u32(&bars->s_free[prev]), (ns[prev] - 1) & 1, abort, kErrWaitMma + 12 + prev);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
-                issue_pv(cv, j > 0);
-                if (next_s)
-                    issue_s(ck);                             // ordered after this P V
-                *turn = seq + 1;                             // hand over first, then commit
-                seq += (t == 0) ? 2 : 1;                     // past tile 1's turn too
-                if (next_s)
-                    mma_commit(smem_u32(&bars->s_full[t]));
-                mma_commit(smem_u32(&bars->v_empty[cv % NV]));
-                if (j == nt - 1)
-                    mma_commit(smem_u32(&bars->o_full[t]));
-                if (next_s) {
-                    if (j + 2 == nt)
-                        mma_commit(smem_u32(&bars->q_empty[t]));
-                    mma_commit(smem_u32(&bars->k_empty[ck % NK]));
+                const uint32_t q_lo = ((sQ + t * L::kTileBytes) >> 4) | (1u << 16);
+                const uint32_t k_lo = k_lo0 + (ck % NK) * kTileUnits;
+#pragma unroll
+                for (int kk = 0; kk < L::kSSteps; ++kk) {
+                    const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
+                    if constexpr (KIND == kE4M3)
+                        mma_f8_ss(s_tmem, desc_join(desc_hi, q_lo + off), desc_join(desc_hi, k_lo + off), idesc_s,
+                                  kk > 0);
+                    else
+                        mma_f16_ss(s_tmem, desc_join(desc_hi, q_lo + off), desc_join(desc_hi, k_lo + off), idesc_s,
+                                   kk > 0);
                 }
-            } else {
-                // tile 0 past its last key tile (causal): no turn; release V_j
-                // (and K_{j+1} below) once they have landed
-                if (!(ok = wait_v(cv)))
-                    break;
-                mbar_arrive(smem_u32(&bars->v_empty[cv % NV]));
-                seq += 1;                                    // tile 1's turn
+                mma_commit(smem_u32(&bars->s_full[t]));
+                if (j == w.n_kv[t] - 1)
+                    mma_commit(smem_u32(&bars->q_empty[t]));
+                ++ns[t];
+                prev = t;
             }
-            ++cv;
-            if (j + 1 < n) {
-                if (!next_s) {
-                    if (!(ok = wait_k(ck)))
-                        break;
-                    mbar_arrive(smem_u32(&bars->k_empty[ck % NK]));
-                }
-                ++ck;
-            }
+            if (!ok)
+                break;
+            mma_commit(smem_u32(&bars->k_empty[ck % NK]));
+            ++ck;
         }
         ++units;
     }
     // every MMA this thread issued completes before TMEM is released
-    mma_commit(smem_u32(&bars->drain[t]));
-    drain_wait(smem_u32(&bars->drain[t]), 0);
+    mma_commit(smem_u32(&bars->drain[2]));
+    drain_wait(smem_u32(&bars->drain[2]), 0);
 }
 
-// MMA issue for E4M3 with P in shared memory: one thread per Q tile (thread 0
-// of warp 9 for tile 0, of warp 10 for tile 1).
-//
-// P_t does not alias S here, so the next S needs only that the softmax has
-// read the previous one out of TMEM (s_free), not that P_t V_j has run; each
-// softmax warpgroup goes from one key tile to the next without waiting for
-// its P V.  The two Q tiles take turns in one S region, in the order
-// S_0(0), S_1(0), S_0(1), S_1(1), ... (tile 0 drops out after its last
-// causal key tile).  Each softmax warpgroup signals s_free[t] when it has
-// read its S; before each S a thread waits for the read of the S that
-// precedes it in that order, counting both tiles' S tiles so far.  That S
-// was itself issued only after its own predecessor had been read, so a
-// waiter is never two phases ahead of the barrier it waits on.  Per Q tile the issue order
-// is S_t(0), then per key tile j: S_t(j+1), P_t V_j and P_t x ones (the row
-// sum).  Both threads release every K / V slot of the unit (barrier count
-// 2), tile 0 also the causal key tile it does not visit.
-template <int D, int NK, int NV>
-__device__ __forceinline__ void mma_issue_fp8(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
-                                              uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV, uint32_t sP,
-                                              uint32_t sOnes, int t)
+// O_t (+)= P_t V_j for Q tile t, kKeysPerStep keys per MMA.  16-bit P_t is
+// read from its TMEM columns (8 columns per step of 16 keys).  E4M3 P_t
+// (K-major, keys contiguous) comes from shared memory, and l_t (+)= P_t x
+// ones.  Both P V threads release every V slot of the unit (barrier count 2),
+// tile 0 also the causal key tile it does not visit.
+template <int D, int KIND, int NK, int NV>
+__device__ __forceinline__ void mma_issue_pv(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
+                                             uint32_t tmem, uint32_t sV, uint32_t sP, uint32_t sOnes, int t)
 {
-    using L = Layout<D, kE4M3>;
-    constexpr uint32_t idesc_s = idesc_make(0u, kBlockM, kBlockN, false);   // E4M3 x E4M3 -> f32
-    constexpr uint32_t idesc_o = idesc_make(0u, kBlockM, D, true);
-    constexpr uint32_t idesc_l = idesc_make(0u, kBlockM, 16, false);
+    using L = Layout<D, KIND>;
+    constexpr bool kFP8 = (KIND == kE4M3);
+    constexpr uint32_t kFmt = (KIND == kBF16) ? 1u : 0u;
+    constexpr uint32_t idesc_o = idesc_make(kFmt, kBlockM, D, true);
+    constexpr uint32_t idesc_l = idesc_make(kFmt, kBlockM, 16, false);
     constexpr uint32_t kTileUnits = L::kTileBytes >> 4;
-    const uint32_t s_tmem = tmem + L::tmem_s(t);
+    const uint32_t p_tmem = tmem + L::tmem_p(t);
     const uint32_t o_tmem = tmem + L::tmem_o(t);
     const uint32_t l_tmem = tmem + L::tmem_l(t);
-    uint32_t ck = 0, cv = 0;             // K / V ring positions at the start of the unit
-    uint32_t sbase[2] = {0, 0};          // S tiles of Q tile 0 / 1 before this unit
-    uint32_t npv = 0;                    // P V groups issued for this Q tile
-    uint32_t units = 0;
-    bool ok = true;
-
-    // Descriptors as (hi, lo) halves (see mma_issue_pair).  P and the ones
-    // tile have 128-byte rows: one 128-byte swizzle span, 8-row groups 1024
-    // bytes apart.
     const uint32_t desc_hi = (uint32_t)(smem_desc(0, 16, L::kSbo, L::kSwzCode) >> 32);
     const uint32_t p_hi = (uint32_t)(smem_desc(0, 16, 1024, 2u) >> 32);
-    const uint32_t q_lo = ((sQ + t * L::kTileBytes) >> 4) | (1u << 16);
-    const uint32_t k_lo0 = (sK >> 4) | (1u << 16);
     const uint32_t v_lo0 = (sV >> 4) | ((uint32_t)(L::kChunkBytes >> 4) << 16);
     const uint32_t p_lo = ((sP + t * L::kPTileBytes) >> 4) | (1u << 16);
     const uint32_t ones_lo = (sOnes >> 4) | (1u << 16);
-
-    auto wait_k = [&](uint32_t kpos) {
-        return wait_bar(smem_u32(&bars->k_full[kpos % NK]), (kpos / NK) & 1, abort, kErrWaitMma + 3);
-    };
-    auto wait_v = [&](uint32_t vpos) {
-        return wait_bar(smem_u32(&bars->v_full[vpos % NV]), (vpos / NV) & 1, abort, kErrWaitMma + 5);
-    };
-    // S_t(j) = Q_t K_j^T into the S region, once K_j has landed and the S
-    // before it in the region's sequence has been read out.
-    auto issue_s = [&](const Unit& w, int j) -> bool {
-        const uint32_t kpos = ck + j;
-        // the S before this one in the region: S_1(j-1) for tile 0, S_0(j)
-        // for tile 1 while tile 0 still has key tiles, else S_1(j-1); as a
-        // count of that tile's S tiles read so far (0: none to wait for)
-        const int pt = (t == 1 && j < w.n_kv[0]) ? 0 : 1;
-        const uint32_t need = sbase[pt] + (uint32_t)((pt == 0) ? j + 1 : j);
-        bool r = wait_k(kpos);
-        if (r && j == 0)
-            r = wait_bar(smem_u32(&bars->q_full[t]), units & 1, abort, kErrWaitMma + 1 + t);
-        if (r && need > 0)
-            r = wait_bar(smem_u32(&bars->s_free[pt]), (need - 1) & 1, abort, kErrWaitMma + 12 + t);
-        if (!r)
-            return false;
-        tc_fence_after_sync();
-        const uint32_t k_lo = k_lo0 + (kpos % NK) * kTileUnits;
-#pragma unroll
-        for (int kk = 0; kk < L::kSSteps; ++kk) {
-            const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
-            mma_f8_ss(s_tmem, desc_join(desc_hi, q_lo + off), desc_join(desc_hi, k_lo + off), idesc_s, kk > 0);
-        }
-        mma_commit(smem_u32(&bars->s_full[t]));
-        if (j == w.n_kv[t] - 1)
-            mma_commit(smem_u32(&bars->q_empty[t]));
-        mma_commit(smem_u32(&bars->k_empty[kpos % NK]));
-        return true;
-    };
-    // O_t (+)= P_t V_j and l_t (+)= P_t ones: P_t (K-major, keys contiguous),
-    // V_j (MN-major) and the ones tile (K-major) from shared memory, 32 keys
-    // per MMA.
-    auto issue_pv = [&](const Unit& w, int j) -> bool {
-        const uint32_t vpos = cv + j;
-        bool r = wait_v(vpos) && wait_bar(smem_u32(&bars->p_full[t]), npv & 1, abort, kErrWaitMma + 6 + t);
-        if (r && j == 0 && units > 0)
-            r = wait_bar(smem_u32(&bars->o_empty[t]), (units - 1) & 1, abort, kErrWaitMma + 8 + t);
-        if (!r)
-            return false;
-        tc_fence_after_sync();
-        const uint32_t v_lo = v_lo0 + (vpos % NV) * kTileUnits;
-#pragma unroll
-        for (int kk = 0; kk < L::kPVSteps; ++kk) {
-            const uint32_t off_p = (uint32_t)((kk * 32) >> 4);
-            const uint32_t off_v = (uint32_t)((kk * L::kKeysPerStep * L::kSwz) >> 4);
-            mma_f8_ss(o_tmem, desc_join(p_hi, p_lo + off_p), desc_join(desc_hi, v_lo + off_v), idesc_o,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < L::kPVSteps; ++kk) {
-            const uint32_t off = (uint32_t)((kk * 32) >> 4);
-            mma_f8_ss(l_tmem, desc_join(p_hi, p_lo + off), desc_join(p_hi, ones_lo + off), idesc_l,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&bars->pv_done[t]));
-        mma_commit(smem_u32(&bars->v_empty[vpos % NV]));
-        if (j == w.n_kv[t] - 1)
-            mma_commit(smem_u32(&bars->o_full[t]));
-        ++npv;
-        return true;
-    };
-
+    uint32_t cv = 0;                     // V ring position
+    uint32_t npv = 0;                    // P V groups issued
+    uint32_t units = 0;
+    bool ok = true;
     for (int r = 0; ok; ++r) {
         const int u = unit_of_round(p, r);
         if (u == -2)
@@ -535,29 +370,47 @@ __device__ __forceinline__ void mma_issue_fp8(const Params& p, Barriers<NK, NV>*
         if (u < 0)
             continue;
         const Unit w = decode_unit(p, u);
-        const int n = w.n_kv[1];         // K/V tiles loaded for the unit (tile 1 sees the most)
-        const int nt = w.n_kv[t];        // of which this Q tile uses the first nt
-        ok = issue_s(w, 0);
-        for (int j = 0; ok && j < nt; ++j) {
-            if (j + 1 < nt)
-                ok = issue_s(w, j + 1);
-            ok = ok && issue_pv(w, j);
-        }
-        // key tiles this Q tile does not visit (tile 0, causal): release them
-        for (int j = nt; ok && j < n; ++j) {
-            ok = wait_k(ck + j) && wait_v(cv + j);
-            if (ok) {
-                mbar_arrive(smem_u32(&bars->k_empty[(ck + j) % NK]));
-                mbar_arrive(smem_u32(&bars->v_empty[(cv + j) % NV]));
+        const int n = w.n_kv[1];
+        const int nt = w.n_kv[t];
+        for (int j = 0; ok && j < n; ++j, ++cv) {
+            ok = wait_bar(smem_u32(&bars->v_full[cv % NV]), (cv / NV) & 1, abort, kErrWaitMma + 5);
+            if (!ok)
+                break;
+            if (j >= nt) {               // tile 0 past its last causal key tile: release V_j
+                mbar_arrive(smem_u32(&bars->v_empty[cv % NV]));
+                continue;
             }
+            ok = wait_bar(smem_u32(&bars->p_full[t]), npv & 1, abort, kErrWaitMma + 6 + t);
+            if (ok && j == 0 && units > 0)
+                ok = wait_bar(smem_u32(&bars->o_empty[t]), (units - 1) & 1, abort, kErrWaitMma + 8 + t);
+            if (!ok)
+                break;
+            tc_fence_after_sync();
+            const uint32_t v_lo = v_lo0 + (cv % NV) * kTileUnits;
+#pragma unroll
+            for (int kk = 0; kk < L::kPVSteps; ++kk) {
+                const uint32_t off_v = (uint32_t)((kk * L::kKeysPerStep * L::kSwz) >> 4);
+                const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                if constexpr (kFP8)
+                    mma_f8_ss(o_tmem, desc_join(p_hi, p_lo + (uint32_t)(kk * 2)), desc_join(desc_hi, v_lo + off_v),
+                              idesc_o, acc);
+                else
+                    mma_f16_ts(o_tmem, p_tmem + kk * 8, desc_join(desc_hi, v_lo + off_v), idesc_o, acc);
+            }
+            if constexpr (kFP8) {
+#pragma unroll
+                for (int kk = 0; kk < L::kPVSteps; ++kk)
+                    mma_f8_ss(l_tmem, desc_join(p_hi, p_lo + (uint32_t)(kk * 2)),
+                              desc_join(p_hi, ones_lo + (uint32_t)(kk * 2)), idesc_l, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&bars->pv_done[t]));
+            mma_commit(smem_u32(&bars->v_empty[cv % NV]));
+            if (j == nt - 1)
+                mma_commit(smem_u32(&bars->o_full[t]));
+            ++npv;
         }
-        ck += n;
-        cv += n;
-        sbase[0] += (uint32_t)w.n_kv[0];
-        sbase[1] += (uint32_t)w.n_kv[1];
         ++units;
     }
-    // every MMA this thread issued completes before TMEM is released
     mma_commit(smem_u32(&bars->drain[t]));
     drain_wait(smem_u32(&bars->drain[t]), 0);
 }
@@ -572,7 +425,6 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     constexpr bool kOutBF16 = (KIND != kFP16);         // E4M3 inputs give a bf16 output
     constexpr int NK = L::kStagesK;
     constexpr int NV = L::kStagesV;
-    constexpr uint32_t kIssuers = 2;                   // MMA-issuing threads, one per Q tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     auto* bars = reinterpret_cast<Barriers<NK, NV>*>(smem + L::kOffBar);
@@ -598,17 +450,16 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         for (int s = 0; s < NK; ++s) {
             mbar_init(smem_u32(&bars->k_full[s]), 1);
-            mbar_init(smem_u32(&bars->k_empty[s]), kIssuers);   // released by every issuing thread
+            mbar_init(smem_u32(&bars->k_empty[s]), 1);          // released by the S issuer
         }
         for (int s = 0; s < NV; ++s) {
             mbar_init(smem_u32(&bars->v_full[s]), 1);
-            mbar_init(smem_u32(&bars->v_empty[s]), kIssuers);
+            mbar_init(smem_u32(&bars->v_empty[s]), 2);          // released by both P V issuers
         }
         mbar_init(smem_u32(&bars->s_free[0]), 128);
         mbar_init(smem_u32(&bars->s_free[1]), 128);
-        mbar_init(smem_u32(&bars->drain[0]), 1);
-        mbar_init(smem_u32(&bars->drain[1]), 1);
-        bars->turn = 0;
+        for (int i = 0; i < 3; ++i)
+            mbar_init(smem_u32(&bars->drain[i]), 1);
         bars->abort = 0;
         fence_mbar_init();
     }
@@ -695,14 +546,14 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     drain_wait(smem_u32(&bars->v_full[i % NV]), (i / NV) & 1);
             }
         }
+      } else if (warp == kSMmaWarp) {
+        // ============================= S issuer =============================
+        if (lane == 0)
+            mma_issue_s<D, KIND, NK, NV>(p, bars, abort, tmem, sQ, sK);
       } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-        // =========================== MMA issuers ============================
+        // =========================== P V issuers ============================
         if (lane == 0) {
-            if constexpr (kFP8)
-                mma_issue_fp8<D, NK, NV>(p, bars, abort, tmem, sQ, sK, sV, sP, smem_u32(smem + L::kOffOnes),
-                                         warp - kMmaWarp);
-            else
-                mma_issue_pair<D, KIND, NK, NV>(p, bars, abort, tmem, sQ, sK, sV, warp - kMmaWarp);
+            mma_issue_pv<D, KIND, NK, NV>(p, bars, abort, tmem, sV, sP, smem_u32(smem + L::kOffOnes), warp - kMmaWarp);
         }
       }
     } else {
@@ -716,11 +567,12 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t o_tmem = tmem + lane_addr + L::tmem_o(t);
         const float c = p.scale_log2;
         uint32_t cs = 0;                                   // S tiles consumed
-        uint32_t np = 0;                                   // E4M3: P tiles handed to the MMA
+        uint32_t np = 0;                                   // P tiles handed to the MMA
         uint32_t units = 0;
         bool ok = true;
         const uint32_t p_row = sP + t * L::kPTileBytes + row * 128;   // E4M3: this row of P_t
         const uint32_t l_tmem = tmem + lane_addr + L::tmem_l(t);      // E4M3: row sum of P_t
+        const uint32_t p_tmem = tmem + lane_addr + L::tmem_p(t);      // 16-bit: P_t
         // O_t *= alpha in TMEM (the running max grew past the threshold)
         auto rescale_o = [&](float alpha) {
 #pragma unroll
@@ -756,11 +608,9 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tc_fence_after_sync();
                 uint32_t r[128];
                 tmem_ld128_wait(s_tmem, s_tmem + 32, s_tmem + 64, s_tmem + 96, r);
-                if constexpr (kFP8) {
-                    // E4M3: the S region is free for the next S as soon as it is read
-                    tc_fence_before_sync();
-                    mbar_arrive(smem_u32(&bars->s_free[t]));
-                }
+                // the S region is free for the next S as soon as it is read
+                tc_fence_before_sync();
+                mbar_arrive(smem_u32(&bars->s_free[t]));
                 const int k0 = j * kBlockN;
                 if (k0 + kBlockN - 1 > limit) {
 #pragma unroll
@@ -796,35 +646,38 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     // argument, packed adds for the fp32 row sum
                     const uint64_t nm2 = f32x2(-m, -m);
                     uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
+                    uint32_t pk[2][32];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t pk[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int e = 64 * h + 2 * i;
-                            float x0, x1;
-                            f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2),
-                                        x0, x1);
-                            const float p0 = ex2_approx(x0);
-                            const float p1 = ex2_approx(x1);
-                            if (i & 1)
-                                acc1 = add_f32x2(acc1, f32x2(p0, p1));
-                            else
-                                acc0 = add_f32x2(acc0, f32x2(p0, p1));
-                            pk[i] = pack2<kOutBF16>(p0, p1);
-                        }
-                        tmem_st32(s_tmem + 32 * h, pk);
+                    for (int i = 0; i < 64; ++i) {
+                        float x0, x1;
+                        f32x2_split(fma_f32x2(f32x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c2, nm2),
+                                    x0, x1);
+                        const float p0 = ex2_approx(x0);
+                        const float p1 = ex2_approx(x1);
+                        if (i & 1)
+                            acc1 = add_f32x2(acc1, f32x2(p0, p1));
+                        else
+                            acc0 = add_f32x2(acc0, f32x2(p0, p1));
+                        pk[i >> 5][i & 31] = pack2<kOutBF16>(p0, p1);
                     }
-                    float sa, sb;
-                    f32x2_split(add_f32x2(acc0, acc1), sa, sb);
-                    l = l * alpha + (sa + sb);
-                    // O_t holds the sum up to tile j-1 (its last P V completed
-                    // before S_t(j) did); rescale it before P_t(j) V_j accumulates.
+                    // the previous P_t V has read P_t's columns and updated O_t
+                    if (np > 0)
+                        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[t]), (np - 1) & 1, abort,
+                                                              kErrWaitSoftmax + 5 + t));
+                    if (!ok)
+                        break;
+                    ++np;
+                    tc_fence_after_sync();
                     if (__any_sync(0xffffffffu, rescale))
                         rescale_o(alpha);
+                    tmem_st32(p_tmem, pk[0]);
+                    tmem_st32(p_tmem + 32, pk[1]);
                     tmem_st_wait();
                     tc_fence_before_sync();
                     mbar_arrive(smem_u32(&bars->p_full[t]));
+                    float sa, sb;
+                    f32x2_split(add_f32x2(acc0, acc1), sa, sb);
+                    l = l * alpha + (sa + sb);
                 } else {
                     // P8 = E4M3(exp2(S*c - m) * 56), four keys per 32-bit word
                     const float bias = m - kLog2P8Scale;
