@@ -125,14 +125,20 @@ struct Layout {
     static constexpr int kBarBytes = 1024;
     static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;     // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    // TMEM columns.  Both Q tiles take turns in one S region (columns 0..127).
-    // 16-bit kinds: P_t in columns 128 + 64 t (two values per column).  E4M3:
-    // P is in shared memory and columns 128 + 16 t hold the row sums l_t (16
-    // columns each, all equal).  O_t in columns 256 + 128 t.
-    __host__ __device__ static constexpr uint32_t tmem_s(int) { return 0u; }
-    __host__ __device__ static constexpr uint32_t tmem_p(int t) { return 128u + 64u * t; }  // 16-bit kinds
-    __host__ __device__ static constexpr uint32_t tmem_l(int t) { return 128u + 16u * t; }  // E4M3
-    __host__ __device__ static constexpr uint32_t tmem_o(int t) { return 256u + 128u * t; } // O_t
+    // TMEM columns (512).  O_t takes the last 2 x D columns.  Both Q tiles
+    // take turns in one S region (columns 0..127), except for 16-bit kinds at
+    // D = 64, where each has its own (128 t).  (E4M3 keeps the shared region
+    // at D = 64 too: it staggers the two softmax warpgroups, whose exp phases
+    // otherwise collide on the MUFU.)  After the S columns: 16-bit P_t (64
+    // columns each, two values per column) or, for E4M3 (P in shared memory),
+    // the row sums l_t (16 columns each, all equal).
+    static constexpr bool kSharedS = (D > 64) || (KIND == kE4M3);
+    static constexpr uint32_t kAfterS = kSharedS ? 128u : 256u;
+    __host__ __device__ static constexpr uint32_t tmem_s(int t) { return kSharedS ? 0u : 128u * t; }
+    __host__ __device__ static constexpr uint32_t tmem_p(int t) { return kAfterS + 64u * t; }  // 16-bit kinds
+    __host__ __device__ static constexpr uint32_t tmem_l(int t) { return kAfterS + 16u * t; }  // E4M3
+    __host__ __device__ static constexpr uint32_t tmem_o(int t) { return 512u - 2u * D + (uint32_t)D * t; }
+    static_assert(kAfterS + 128u <= 512u - 2u * D, "TMEM columns overlap");
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -278,7 +284,6 @@ __device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* b
     constexpr uint32_t kFmt = (KIND == kBF16) ? 1u : 0u;          // bf16 / f16 / E4M3
     constexpr uint32_t idesc_s = idesc_make(kFmt, kBlockM, kBlockN, false);
     constexpr uint32_t kTileUnits = L::kTileBytes >> 4;
-    const uint32_t s_tmem = tmem + L::tmem_s(0);
     const uint32_t desc_hi = (uint32_t)(smem_desc(0, 16, L::kSbo, L::kSwzCode) >> 32);
     const uint32_t k_lo0 = (sK >> 4) | (1u << 16);
     uint32_t ck = 0;                     // K ring position
@@ -301,8 +306,11 @@ __device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* b
                     continue;
                 if (j == 0)
                     ok = wait_bar(smem_u32(&bars->q_full[t]), units & 1, abort, kErrWaitMma + 1 + t);
-                if (ok && prev >= 0)         // the previous S has been read out of the region
-                    ok = wait_bar(smem_u32(&bars->s_free[prev]), (ns[prev] - 1) & 1, abort, kErrWaitMma + 12 + prev);
+                // the previous S in this region has been read out of it: the
+                // last S of either tile (shared region) or of this tile
+                const int pt = L::kSharedS ? prev : (ns[t] > 0 ? t : -1);
+                if (ok && pt >= 0)
+                    ok = wait_bar(smem_u32(&bars->s_free[pt]), (ns[pt] - 1) & 1, abort, kErrWaitMma + 12 + pt);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
@@ -311,6 +319,7 @@ __device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* b
 #pragma unroll
                 for (int kk = 0; kk < L::kSSteps; ++kk) {
                     const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
+                    const uint32_t s_tmem = tmem + L::tmem_s(t);
                     if constexpr (KIND == kE4M3)
                         mma_f8_ss(s_tmem, desc_join(desc_hi, q_lo + off), desc_join(desc_hi, k_lo + off), idesc_s,
                                   kk > 0);
