@@ -54,10 +54,10 @@ def _bind(lib):
     cvp, cl, ci, cd = ctypes.c_void_p, ctypes.c_long, ctypes.c_int, ctypes.c_double
     lib.oracle_sdpa_rows.restype = ci
     lib.oracle_sdpa_rows.argtypes = [cvp, cvp, cvp, ci, cd, cd, cd, cl, cl, cl, cl, cl, cl,
-                                     cd, ci, cvp, cl, cvp, cvp, ci]
+                                     cd, ci, cvp, cl, cvp, cvp, cvp, ci]
     lib.oracle_sdpa_fwd.restype = ci
     lib.oracle_sdpa_fwd.argtypes = [cvp, cvp, cvp, ci, cd, cd, cd, cl, cl, cl, cl, cl, cl,
-                                    cd, ci, cvp, ci]
+                                    cd, ci, cvp, cvp, ci]
     lib.oracle_decode.restype = cd
     lib.oracle_decode.argtypes = [cvp, cl, ci, cd]
     lib.oracle_max_threads.restype = ci
@@ -113,7 +113,7 @@ def _check_shapes(q, k, v):
 
 def sdpa_reference(q, k, v, *, causal: bool, scale: float | None = None, dtype: str = "bf16",
                    descales=(1.0, 1.0, 1.0), rows=None, threads: int = 0,
-                   return_weights: bool = False, lib=None):
+                   return_weights: bool = False, return_lse: bool = False, lib=None):
     """fp64 attention output.
 
     q: [B, Sq, Hq, D]; k, v: [B, Skv, Hkv, D] (numpy or CPU torch), holding
@@ -124,8 +124,11 @@ def sdpa_reference(q, k, v, *, causal: bool, scale: float | None = None, dtype: 
     Returns float64 [B, Sq, Hq, D], or, when ``rows`` (flat indices
     (b*Sq + i)*Hq + hq) is given, float64 [len(rows), D].  With
     ``return_weights`` (rows required) also returns the [len(rows), Skv]
-    softmax weights.  :func:`last_threads` reports how many threads the call
-    used.
+    softmax weights.  With ``return_lse`` also returns the log-sum-exp of each
+    row's visible scores, log(sum_j exp(s_j)) -- the log of the softmax
+    denominator of section 1 -- as float64 [B, Hq, Sq] (whole pass) or
+    [len(rows)] (rows); with both flags the order is (out, weights, lse).
+    :func:`last_threads` reports how many threads the call used.
     """
     lib = lib or load_library()
     qa, ka, va = _raw(q, dtype), _raw(k, dtype), _raw(v, dtype)
@@ -139,24 +142,28 @@ def sdpa_reference(q, k, v, *, causal: bool, scale: float | None = None, dtype: 
         if return_weights:
             raise ValueError("return_weights needs explicit rows")
         out = np.empty((B, Sq, Hq, D), dtype=np.float64)
+        lse = np.empty((B, Hq, Sq), dtype=np.float64) if return_lse else None
         nt = lib.oracle_sdpa_fwd(qa.ctypes.data, ka.ctypes.data, va.ctypes.data, code, dq, dk, dv,
                                  B, Hq, Hkv, Sq, Skv, D, float(scale), int(bool(causal)),
-                                 out.ctypes.data, int(threads))
+                                 out.ctypes.data, lse.ctypes.data if lse is not None else None, int(threads))
         if nt < 0:
             raise ValueError("oracle rejected the arguments")
         _last_threads = nt
-        return out
+        return (out, lse) if return_lse else out
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     out = np.empty((r.size, D), dtype=np.float64)
     w = np.empty((r.size, Skv), dtype=np.float64) if return_weights else None
+    lse = np.empty((r.size,), dtype=np.float64) if return_lse else None
     nt = lib.oracle_sdpa_rows(qa.ctypes.data, ka.ctypes.data, va.ctypes.data, code, dq, dk, dv,
                               B, Hq, Hkv, Sq, Skv, D, float(scale), int(bool(causal)),
                               r.ctypes.data, r.size, out.ctypes.data,
-                              w.ctypes.data if w is not None else None, int(threads))
+                              w.ctypes.data if w is not None else None,
+                              lse.ctypes.data if lse is not None else None, int(threads))
     if nt < 0:
         raise ValueError("oracle rejected the arguments")
     _last_threads = nt
-    return (out, w) if return_weights else out
+    res = (out,) + ((w,) if return_weights else ()) + ((lse,) if return_lse else ())
+    return res[0] if len(res) == 1 else res
 
 
 _last_threads = 0

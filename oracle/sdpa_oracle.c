@@ -134,10 +134,12 @@ static long bshd(long b, long s, long h, long d, long S, long H, long D)
  * Output row (b, i, hq):  scores s_j = scale * sum_d Q[b,i,hq,d] K[b,j,g,d]
  * for the visible keys j, weights w_j = exp(s_j - max s) / sum exp(s - max s),
  * out = sum_j w_j V[b,j,g,:].  Masked keys get weight 0.  `scores` is scratch
- * of Skv doubles; `w_out` (optional) receives all Skv weights.
+ * of Skv doubles; `w_out` (optional) receives all Skv weights; `lse_out`
+ * (optional) receives log(sum_j exp(s_j)) over the visible keys, the log of
+ * the softmax denominator, formed as max s + log(sum exp(s - max s)).
  */
 static void attend_row(const problem_t *p, long b, long hq, long i,
-                       double *scores, double *out, double *w_out)
+                       double *scores, double *out, double *w_out, double *lse_out)
 {
     const long G = p->Hq / p->Hkv;          /* query heads per KV head */
     const long g = hq / G;                  /* KV head read by query head hq */
@@ -166,6 +168,8 @@ static void attend_row(const problem_t *p, long b, long hq, long i,
         scores[j] = exp(scores[j] - m);
         denom += scores[j];
     }
+    if (lse_out)
+        *lse_out = m + log(denom);
     for (long j = 0; j < n_vis; ++j)
         scores[j] /= denom;
 
@@ -205,14 +209,15 @@ static int resolve_threads(int nthreads)
 /*
  * Compute the output rows listed in `rows` (flat indices r = (b*Sq + i)*Hq + hq
  * into the [B][Sq][Hq] row space of O); row k of `out` (D doubles) receives
- * row rows[k].  If `weights` is non-NULL it receives nrows x Skv weights.
- * Returns the number of threads used, or -1 on an invalid argument.
+ * row rows[k].  If `weights` is non-NULL it receives nrows x Skv weights, if
+ * `lse` is non-NULL it receives the nrows log-sum-exp values.  Returns the
+ * number of threads used, or -1 on an invalid argument.
  */
 int oracle_sdpa_rows(const void *Q, const void *K, const void *V, int dtype,
                      double descale_q, double descale_k, double descale_v,
                      long B, long Hq, long Hkv, long Sq, long Skv, long D,
                      double scale, int causal, const long *rows, long nrows,
-                     double *out, double *weights, int nthreads)
+                     double *out, double *weights, double *lse, int nthreads)
 {
     problem_t p = {Q, K, V, dtype, descale_q, descale_k, descale_v,
                    B, Hq, Hkv, Sq, Skv, D, scale, causal};
@@ -239,7 +244,7 @@ int oracle_sdpa_rows(const void *Q, const void *K, const void *V, int dtype,
             long i = (r / Hq) % Sq;
             long b = r / (Hq * Sq);
             attend_row(&p, b, hq, i, scores, out + k * D,
-                       weights ? weights + k * Skv : NULL);
+                       weights ? weights + k * Skv : NULL, lse ? lse + k : NULL);
         }
         free(scores);
     }
@@ -247,13 +252,14 @@ int oracle_sdpa_rows(const void *Q, const void *K, const void *V, int dtype,
 }
 
 /*
- * Whole forward pass: out is [B][Sq][Hq][D] doubles.  Returns the number of
- * threads used, or -1 on an invalid argument.
+ * Whole forward pass: out is [B][Sq][Hq][D] doubles; `lse` (optional) is
+ * [B][Hq][Sq] doubles.  Returns the number of threads used, or -1 on an
+ * invalid argument.
  */
 int oracle_sdpa_fwd(const void *Q, const void *K, const void *V, int dtype,
                     double descale_q, double descale_k, double descale_v,
                     long B, long Hq, long Hkv, long Sq, long Skv, long D,
-                    double scale, int causal, double *out, int nthreads)
+                    double scale, int causal, double *out, double *lse, int nthreads)
 {
     problem_t p = {Q, K, V, dtype, descale_q, descale_k, descale_v,
                    B, Hq, Hkv, Sq, Skv, D, scale, causal};
@@ -276,7 +282,8 @@ int oracle_sdpa_fwd(const void *Q, const void *K, const void *V, int dtype,
             long hq = r % Hq;
             long i = (r / Hq) % Sq;
             long b = r / (Hq * Sq);
-            attend_row(&p, b, hq, i, scores, out + r * D, NULL);
+            attend_row(&p, b, hq, i, scores, out + r * D, NULL,
+                       lse ? lse + (b * Hq + hq) * Sq + i : NULL);
         }
         free(scores);
     }

@@ -42,8 +42,45 @@ def pin_hand_cases(lib):
         q = np.array(c["q"], dtype=np.float64)[None, :, None, :]
         k = np.array(c["k"], dtype=np.float64)[None, :, None, :]
         v = np.array(c["v"], dtype=np.float64)[None, :, None, :]
-        o = ref(lib, q, k, v, causal=c["causal"], scale=c["scale"], dtype="f64")
+        o, lse = ref(lib, q, k, v, causal=c["causal"], scale=c["scale"], dtype="f64", return_lse=True)
         np.testing.assert_allclose(o[0, :, 0, :], np.array(c["o"]), rtol=0, atol=1e-12, err_msg=c["name"])
+        np.testing.assert_allclose(lse[0, 0, :], np.array(c["lse"]), rtol=0, atol=1e-12, err_msg=c["name"])
+
+
+def pin_lse_closed_forms(lib):
+    # Q = 0: every visible score is 0, so log sum exp = log(number of visible keys)
+    Sq, Skv = 9, 12
+    q, k, v = np.zeros((1, Sq, 2, 8)), rnd(60, 1, Skv, 1, 8), rnd(61, 1, Skv, 1, 8)
+    _, lse = ref(lib, q, k, v, causal=False, dtype="f64", return_lse=True)
+    np.testing.assert_allclose(lse, np.full((1, 2, Sq), math.log(Skv)), rtol=0, atol=1e-14)
+    _, lse = ref(lib, q, k, v, causal=True, dtype="f64", return_lse=True)
+    want = np.log(np.minimum(np.arange(Sq) + 1, Skv))
+    np.testing.assert_allclose(lse[0, 0], want, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 1], want, rtol=0, atol=1e-14)
+    # one key: the log sum exp is that key's score, scale * q . k
+    q, k = rnd(62, 1, 3, 1, 4), rnd(63, 1, 1, 1, 4)
+    _, lse = ref(lib, q, k, k, causal=False, scale=0.7, dtype="f64", return_lse=True)
+    np.testing.assert_allclose(lse[0, 0], 0.7 * (q[0, :, 0, :] @ k[0, 0, 0, :]), rtol=0, atol=1e-14)
+    # one key 80 above the rest: log sum exp = that score + log(1 + O(e^-80))
+    q = np.zeros((1, 1, 1, 2)); q[0, 0, 0, 0] = 1.0
+    k = np.zeros((1, 5, 1, 2)); k[0, 3, 0, 0] = 80.0
+    _, lse = ref(lib, q, k, k, causal=False, scale=1.0, dtype="f64", return_lse=True)
+    assert abs(lse[0, 0, 0] - 80.0) < 1e-30 + 5 * math.exp(-80)
+
+
+def pin_lse_scipy_logsumexp(lib):
+    # a library routine for the same quantity: scipy's logsumexp of the
+    # masked score matrix (scores formed here with einsum)
+    from scipy.special import logsumexp
+    q, k, v = rnd(64, 2, 7, 4, 8), rnd(65, 2, 10, 2, 8), rnd(66, 2, 10, 2, 8)
+    scale = 0.37
+    for causal in (False, True):
+        _, lse = ref(lib, q, k, v, causal=causal, scale=scale, dtype="f64", return_lse=True)
+        kr = np.repeat(k, 2, axis=2)                       # query head h reads KV head h // 2
+        s = np.einsum("bihd,bjhd->bhij", q, kr) * scale
+        if causal:
+            s = np.where(np.tril(np.ones((7, 10), dtype=bool))[None, None], s, -np.inf)
+        np.testing.assert_allclose(lse, logsumexp(s, axis=-1), rtol=0, atol=1e-12)
 
 
 def pin_single_key(lib):
@@ -206,7 +243,7 @@ PINS = [pin_hand_cases, pin_single_key, pin_constant_v, pin_zero_query_is_mean,
         pin_causal_first_and_last_rows, pin_causal_rows_are_prefix_attention,
         pin_gqa_equals_repeated_mha, pin_key_permutation_invariance, pin_key_shift_invariance,
         pin_dominant_key_large_logits, pin_weights_rows_sum_to_one, pin_torch_sdpa_float64,
-        pin_e4m3_descales]
+        pin_e4m3_descales, pin_lse_closed_forms, pin_lse_scipy_logsumexp]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -260,6 +297,17 @@ def test_rows_match_full(oracle_lib):
     np.testing.assert_array_equal(part, flat[rows])
 
 
+def test_lse_rows_match_full(oracle_lib):
+    # the row mode's LSE is the whole pass's [B][Hq][Sq] entry of the same row
+    x = make_qkv(52, 2, 4, 2, 33, 40, 16, "bf16")
+    _, full = ref(oracle_lib, x.q, x.k, x.v, causal=True, dtype="bf16", return_lse=True)
+    rows = [0, 7, 33 * 4 + 2, 2 * 33 * 4 - 1]
+    _, part = ref(oracle_lib, x.q, x.k, x.v, causal=True, dtype="bf16", rows=rows, return_lse=True)
+    for r, val in zip(rows, part):
+        hq, i, b = r % 4, (r // 4) % 33, r // (4 * 33)
+        assert val == full[b, hq, i]
+
+
 def test_rejects_bad_arguments(oracle_lib):
     q = np.zeros((1, 4, 3, 8))
     k = np.zeros((1, 4, 2, 8))
@@ -284,6 +332,8 @@ MUTANTS = {
                              "return decode_e4m3(((const uint8_t *)base)[idx]);"),
     "e4m3_bias_off_by_one": ("v = ldexp((double)(8 + f), e - 10);", "v = ldexp((double)(8 + f), e - 9);"),
     "fp16_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    "lse_without_max": ("*lse_out = m + log(denom);", "*lse_out = log(denom);"),
+    "lse_in_log2": ("*lse_out = m + log(denom);", "*lse_out = m + log2(denom);"),
 }
 
 
