@@ -61,9 +61,26 @@ typedef enum {
     SDPA_ERR_DTYPE = 6,        /* unknown dtype, or E4M3 passed to sdpa_fwd */
     SDPA_ERR_SCALE = 7,        /* scale (or a descale) is not finite and > 0 */
     SDPA_ERR_ARCH = 8,         /* current device is not compute capability 10.3 */
-    SDPA_ERR_ALIAS = 9,        /* O overlaps Q, K or V */
-    SDPA_ERR_CUDA = 10         /* a CUDA call failed; see sdpa_last_cuda_error() */
+    SDPA_ERR_ALIAS = 9,        /* O (or LSE) overlaps an input or each other */
+    SDPA_ERR_CUDA = 10,        /* a CUDA call failed; see sdpa_last_cuda_error() */
+    SDPA_ERR_LAYOUT = 11       /* a stride is unusable (see sdpa_layout_t) */
 } sdpa_status_t;
+
+/*
+ * Strides of one [B][S][H][D] tensor, in elements, for the *_ex entry points.
+ * The head dimension D is always contiguous.  Contiguous BSHD (the layout of
+ * sdpa_fwd) is {S*H*D, H*D, D}; BHSD, the (B, N, T, H) layout section 4
+ * ("Implement attention from scratch") transposes Q, K and V into before its
+ * matmuls, is {H*S*D, D, S*D}.
+ * Each stride must be > 0 and a multiple of 16 bytes (8 bf16 / fp16 or 16
+ * E4M3 elements), below 2^40 bytes; O's strides must not map two elements to
+ * one address.
+ */
+typedef struct {
+    long long batch;   /* elements from (b, s, h, 0) to (b + 1, s, h, 0) */
+    long long seq;     /* elements from (b, s, h, 0) to (b, s + 1, h, 0) */
+    long long head;    /* elements from (b, s, h, 0) to (b, s, h + 1, 0) */
+} sdpa_layout_t;
 
 /*
  * Attention forward pass, bf16 or fp16 (section 6: the fused backend takes
@@ -93,13 +110,47 @@ sdpa_status_t sdpa_fwd(const void *Q, const void *K, const void *V, void *O,
  *             quantised with scale 448 / amax(x)).
  *   O         device, bfloat16, [B][Sq][Hq][D].
  *   descale_q, descale_k, descale_v   finite, > 0.
- * The softmax weights P are quantised to E4M3 (times 448) before P V, with an
- * fp32 accumulator; other arguments as for sdpa_fwd.
+ * The softmax weights P are quantised to E4M3 before P V (as P * 56 with
+ * P <= 8: the running max the weights are taken against may trail the row
+ * max by up to a factor 8, and 8 * 56 = 448 is the largest E4M3 value), with
+ * an fp32 accumulator; O is normalised by the sum of those quantised
+ * weights.  Other arguments as for sdpa_fwd.
  */
 sdpa_status_t sdpa_fwd_fp8(const void *Q, const void *K, const void *V, void *O,
                            int B, int Hq, int Hkv, int Sq, int Skv, int D,
                            float scale, float descale_q, float descale_k, float descale_v,
                            int causal, void *stream);
+
+/*
+ * sdpa_fwd with explicit layouts and an optional log-sum-exp output.
+ *   q_layout, k_layout, v_layout, o_layout   host pointers to the strides of
+ *             Q, K, V, O (sdpa_layout_t); NULL means contiguous BSHD.
+ *   LSE       device, fp32 [B][Hq][Sq] contiguous, or NULL: LSE[b][hq][i] =
+ *             log(sum_j exp(s_ij)) over the keys row i sees, s_ij = scale *
+ *             q_i . k_j -- the log of the softmax denominator of section 1,
+ *             which a backward pass or a merge of partial results needs.
+ *             4-byte aligned; must not overlap Q, K, V or O.
+ * Other arguments as for sdpa_fwd; O's elements are written where o_layout
+ * puts them, nothing else in its span is touched.
+ */
+sdpa_status_t sdpa_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                          int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                          const sdpa_layout_t *q_layout, const sdpa_layout_t *k_layout,
+                          const sdpa_layout_t *v_layout, const sdpa_layout_t *o_layout,
+                          float scale, int causal, sdpa_dtype_t dtype, void *stream);
+
+/*
+ * sdpa_fwd_fp8 with explicit layouts and an optional log-sum-exp output
+ * (arguments as for sdpa_fwd_ex and sdpa_fwd_fp8).  The LSE is that of the
+ * dequantised scores, scale * descale_q * descale_k * q8_i . k8_j, with the
+ * row sum taken over the E4M3-rounded weights the kernel multiplies into V.
+ */
+sdpa_status_t sdpa_fwd_fp8_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                              int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                              const sdpa_layout_t *q_layout, const sdpa_layout_t *k_layout,
+                              const sdpa_layout_t *v_layout, const sdpa_layout_t *o_layout,
+                              float scale, float descale_q, float descale_k, float descale_v,
+                              int causal, void *stream);
 
 /* Static, human-readable name of a status code. */
 const char *sdpa_status_string(sdpa_status_t status);
@@ -115,7 +166,7 @@ int sdpa_last_cuda_error(void);
  */
 sdpa_status_t sdpa_device_error(unsigned int *code);
 
-/* Version of this ABI (bumped on any incompatible change). */
+/* Version of this ABI (bumped on any change; 2 added the *_ex entry points). */
 int sdpa_abi_version(void);
 
 #ifdef __cplusplus

@@ -14,7 +14,8 @@ import torch
 from . import _abi
 from ._abi import SdpaError, check, lib, status_string
 
-__all__ = ["sdpa_fwd", "sdpa_fwd_fp8", "sdpa_status_string", "sdpa_device_error", "SdpaError", "lib"]
+__all__ = ["sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_status_string",
+           "sdpa_device_error", "SdpaError", "lib"]
 
 _DTYPE = {torch.bfloat16: _abi.SDPA_DTYPE_BF16, torch.float16: _abi.SDPA_DTYPE_FP16}
 
@@ -77,6 +78,67 @@ def sdpa_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Ten
     check(lib().sdpa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
                              float(scale), float(descale_q), float(descale_k), float(descale_v),
                              int(bool(causal)), _stream_ptr(stream)))
+    return o
+
+
+def _layout(t: torch.Tensor) -> _abi.Layout:
+    """Strides of a [B, S, H, D] tensor view (D contiguous) as sdpa_layout_t."""
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError("tensors must be 4-D [B, S, H, D] views with a contiguous last dimension")
+    return _abi.Layout(t.stride(0), t.stride(1), t.stride(2))
+
+
+def _lse_ptr(lse, B, Hq, Sq):
+    if lse is None:
+        return None
+    if not lse.is_cuda or lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Sq):
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, Hq, Sq]")
+    return lse.data_ptr()
+
+
+def sdpa_fwd_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor | None = None,
+                *, causal: bool = False, scale: float | None = None, stream=None) -> torch.Tensor:
+    """sdpa_fwd on [B, S, H, D] views with any strides the library accepts
+    (e.g. a BHSD tensor permuted to [B, S, H, D]), writing O through ``o``'s
+    strides and, when ``lse`` ([B, Hq, Sq] float32) is given, the log-sum-exp
+    of every row's scores.  Returns ``o``."""
+    for t in (q, k, v, o):
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+    if q.dtype != k.dtype or q.dtype != v.dtype or o.dtype != q.dtype or tuple(o.shape) != tuple(q.shape):
+        raise ValueError("q, k, v, o must share a dtype; o is shaped like q")
+    B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+    if tuple(k.shape) != tuple(v.shape):
+        raise ValueError("K and V must have the same shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lq, lk, lv, lo = _layout(q), _layout(k), _layout(v), _layout(o)
+    check(lib().sdpa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _lse_ptr(lse, B, Hq, Sq),
+                            B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq), ctypes.byref(lk), ctypes.byref(lv),
+                            ctypes.byref(lo), float(scale), int(bool(causal)), _DTYPE.get(q.dtype, 99),
+                            _stream_ptr(stream)))
+    return o
+
+
+def sdpa_fwd_fp8_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                    lse: torch.Tensor | None = None, *, descale_q: float, descale_k: float, descale_v: float,
+                    causal: bool = False, scale: float | None = None, stream=None) -> torch.Tensor:
+    """sdpa_fwd_fp8 with strided views and an optional LSE, as sdpa_fwd_ex."""
+    for t in (q, k, v):
+        if not t.is_cuda or t.element_size() != 1:
+            raise ValueError("inputs must be 1-byte CUDA tensors")
+    if not o.is_cuda or o.dtype != torch.bfloat16 or tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must be a bf16 CUDA tensor shaped like q")
+    B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+    if tuple(k.shape) != tuple(v.shape):
+        raise ValueError("K and V must have the same shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lq, lk, lv, lo = _layout(q), _layout(k), _layout(v), _layout(o)
+    check(lib().sdpa_fwd_fp8_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _lse_ptr(lse, B, Hq, Sq),
+                                B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq), ctypes.byref(lk), ctypes.byref(lv),
+                                ctypes.byref(lo), float(scale), float(descale_q), float(descale_k),
+                                float(descale_v), int(bool(causal)), _stream_ptr(stream)))
     return o
 
 

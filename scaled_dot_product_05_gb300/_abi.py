@@ -10,10 +10,16 @@ from .build import LIB_PATH
 SDPA_DTYPE_BF16, SDPA_DTYPE_FP16, SDPA_DTYPE_E4M3 = 0, 1, 2
 STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_NULL_PTR", 2: "SDPA_ERR_MISALIGNED", 3: "SDPA_ERR_BAD_SHAPE",
           4: "SDPA_ERR_HEADS", 5: "SDPA_ERR_HEAD_DIM", 6: "SDPA_ERR_DTYPE", 7: "SDPA_ERR_SCALE",
-          8: "SDPA_ERR_ARCH", 9: "SDPA_ERR_ALIAS", 10: "SDPA_ERR_CUDA"}
+          8: "SDPA_ERR_ARCH", 9: "SDPA_ERR_ALIAS", 10: "SDPA_ERR_CUDA", 11: "SDPA_ERR_LAYOUT"}
 # every function include/sdpa.h declares
-EXPORTS = ("sdpa_fwd", "sdpa_fwd_fp8", "sdpa_status_string", "sdpa_last_cuda_error",
-           "sdpa_device_error", "sdpa_abi_version")
+EXPORTS = ("sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_status_string",
+           "sdpa_last_cuda_error", "sdpa_device_error", "sdpa_abi_version")
+
+
+class Layout(ctypes.Structure):
+    """sdpa_layout_t: element strides (batch, seq, head) of a [B][S][H][D]
+    tensor whose last dimension is contiguous."""
+    _fields_ = [("batch", ctypes.c_longlong), ("seq", ctypes.c_longlong), ("head", ctypes.c_longlong)]
 
 _lock = threading.Lock()
 _lib = None
@@ -31,6 +37,11 @@ def _bind(lib):
     lib.sdpa_fwd.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
     lib.sdpa_fwd_fp8.restype = i
     lib.sdpa_fwd_fp8.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, f, f, f, i, vp]
+    lp = ctypes.POINTER(Layout)
+    lib.sdpa_fwd_ex.restype = i
+    lib.sdpa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, lp, lp, lp, lp, f, i, i, vp]
+    lib.sdpa_fwd_fp8_ex.restype = i
+    lib.sdpa_fwd_fp8_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, lp, lp, lp, lp, f, f, f, f, i, vp]
     lib.sdpa_status_string.restype = ctypes.c_char_p
     lib.sdpa_status_string.argtypes = [i]
     lib.sdpa_last_cuda_error.restype = i

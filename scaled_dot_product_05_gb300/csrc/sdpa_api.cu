@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -107,23 +108,97 @@ bool aligned16(const void* p)
     return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
-bool overlaps(const void* a, size_t na, const void* b, size_t nb)
+bool overlaps(const void* a, long long na, const void* b, long long nb)
 {
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-    return a0 < b0 + nb && b0 < a0 + na;
+    const unsigned __int128 a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + (unsigned long long)nb && b0 < a0 + (unsigned long long)na;
 }
 
 struct Shape {
     int B, Hq, Hkv, Sq, Skv, D;
 };
 
-// Checks shared by both entry points; no CUDA call.
-sdpa_status_t check_common(const void* Q, const void* K, const void* V, const void* O, const Shape& s,
-                           int in_elem_bytes, int out_elem_bytes)
+// Element strides of a [B][S][H][D] tensor (D contiguous).
+struct Strides {
+    long long b, s, h;
+};
+
+Strides contiguous_bshd(int S, int H, int D)
 {
-    if (!Q || !K || !V || !O)
+    return {static_cast<long long>(S) * H * D, static_cast<long long>(H) * D, D};
+}
+
+Strides resolve(const sdpa_layout_t* l, int S, int H, int D)
+{
+    return l ? Strides{l->batch, l->seq, l->head} : contiguous_bshd(S, H, D);
+}
+
+// Bytes from the first element to one past the last one of a B x S x H x D
+// tensor with strides st (all strides > 0), or -1 past 2^62 bytes.
+long long span_bytes(const Strides& st, int B, int S, int H, int D, int elem_bytes)
+{
+    const __int128 last = (__int128)(B - 1) * st.b + (__int128)(S - 1) * st.s + (__int128)(H - 1) * st.h + D;
+    const __int128 bytes = last * elem_bytes;
+    return bytes > ((__int128)1 << 62) ? -1 : static_cast<long long>(bytes);
+}
+
+// A stride the TMA engine and the 16-byte output stores accept: > 0, a
+// multiple of 16 bytes, below 2^40 bytes.
+bool stride_ok(long long st, int elem_bytes)
+{
+    if (st <= 0 || st > (1ll << 40) / elem_bytes)
+        return false;
+    return (st * elem_bytes) % 16 == 0;
+}
+
+bool strides_ok(const Strides& st, int elem_bytes)
+{
+    return stride_ok(st.b, elem_bytes) && stride_ok(st.s, elem_bytes) && stride_ok(st.h, elem_bytes);
+}
+
+// No two (b, s, h, d) of a B x S x H x D tensor share an address: with the
+// dimensions of size > 1 sorted by stride, each stride reaches past the span
+// of the smaller ones (D contiguous comes first).
+bool injective(const Strides& st, int B, int S, int H, int D)
+{
+    long long dims[3][2] = {{st.b, B}, {st.s, S}, {st.h, H}};
+    for (int i = 0; i < 3; ++i)                      // sort by stride
+        for (int j = i + 1; j < 3; ++j)
+            if (dims[j][0] < dims[i][0]) {
+                std::swap(dims[i][0], dims[j][0]);
+                std::swap(dims[i][1], dims[j][1]);
+            }
+    long long reach = D;                             // span of the dimensions so far
+    for (int i = 0; i < 3; ++i) {
+        if (dims[i][1] == 1)
+            continue;
+        if (dims[i][0] < reach)
+            return false;
+        reach = dims[i][0] * (dims[i][1] - 1) + reach;
+    }
+    return true;
+}
+
+bool aligned(const void* p, unsigned bytes)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0;
+}
+
+struct Args {
+    const void *Q, *K, *V;
+    void* O;
+    float* lse;
+    Shape s;
+    Strides q, k, v, o;
+};
+
+// Checks shared by every entry point; no CUDA call.
+sdpa_status_t check_common(const Args& a, int in_elem_bytes, int out_elem_bytes)
+{
+    const Shape& s = a.s;
+    if (!a.Q || !a.K || !a.V || !a.O)
         return SDPA_ERR_NULL_PTR;
-    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+    if (!aligned16(a.Q) || !aligned16(a.K) || !aligned16(a.V) || !aligned16(a.O) || !aligned(a.lse, 4))
         return SDPA_ERR_MISALIGNED;
     if (s.B < 1 || s.Hq < 1 || s.Hkv < 1 || s.Sq < 1 || s.Skv < 1)
         return SDPA_ERR_BAD_SHAPE;
@@ -135,12 +210,24 @@ sdpa_status_t check_common(const void* Q, const void* K, const void* V, const vo
     const int64_t n_pairs = (static_cast<int64_t>(s.Sq) + sdpa::kUnitRows - 1) / sdpa::kUnitRows;
     if (static_cast<int64_t>(s.B) * s.Hq * n_pairs > INT32_MAX)
         return SDPA_ERR_BAD_SHAPE;
-    const size_t nq = static_cast<size_t>(s.B) * s.Sq * s.Hq * s.D;
-    const size_t nkv = static_cast<size_t>(s.B) * s.Skv * s.Hkv * s.D;
-    const size_t o_bytes = nq * out_elem_bytes;
-    if (overlaps(O, o_bytes, Q, nq * in_elem_bytes) || overlaps(O, o_bytes, K, nkv * in_elem_bytes) ||
-        overlaps(O, o_bytes, V, nkv * in_elem_bytes))
+    if (!strides_ok(a.q, in_elem_bytes) || !strides_ok(a.k, in_elem_bytes) || !strides_ok(a.v, in_elem_bytes) ||
+        !strides_ok(a.o, out_elem_bytes) || !injective(a.o, s.B, s.Sq, s.Hq, s.D))
+        return SDPA_ERR_LAYOUT;
+    const long long q_bytes = span_bytes(a.q, s.B, s.Sq, s.Hq, s.D, in_elem_bytes);
+    const long long k_bytes = span_bytes(a.k, s.B, s.Skv, s.Hkv, s.D, in_elem_bytes);
+    const long long v_bytes = span_bytes(a.v, s.B, s.Skv, s.Hkv, s.D, in_elem_bytes);
+    const long long o_bytes = span_bytes(a.o, s.B, s.Sq, s.Hq, s.D, out_elem_bytes);
+    if (q_bytes < 0 || k_bytes < 0 || v_bytes < 0 || o_bytes < 0)
+        return SDPA_ERR_LAYOUT;
+    if (overlaps(a.O, o_bytes, a.Q, q_bytes) || overlaps(a.O, o_bytes, a.K, k_bytes) ||
+        overlaps(a.O, o_bytes, a.V, v_bytes))
         return SDPA_ERR_ALIAS;
+    if (a.lse) {
+        const long long l_bytes = static_cast<long long>(s.B) * s.Hq * s.Sq * static_cast<long long>(sizeof(float));
+        if (overlaps(a.lse, l_bytes, a.Q, q_bytes) || overlaps(a.lse, l_bytes, a.K, k_bytes) ||
+            overlaps(a.lse, l_bytes, a.V, v_bytes) || overlaps(a.lse, l_bytes, a.O, o_bytes))
+            return SDPA_ERR_ALIAS;
+    }
     return SDPA_OK;
 }
 
@@ -149,11 +236,12 @@ bool valid_scale(float x)
     return std::isfinite(x) && x > 0.f;
 }
 
-// 4-D tensor map over a [B][S][H][D] array: dims (innermost first) {D, H, S, B},
-// box {one swizzle chunk of the row (128 bytes, or 64 when a row is 64 bytes),
-// 1 head, 128 rows, 1 batch}, matching swizzle, zero fill out of bounds
-// (ragged sequence tails).
-bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int D, int H, int S, int B)
+// 4-D tensor map over a [B][S][H][D] tensor with element strides st: dims
+// (innermost first) {D, H, S, B}, box {one swizzle chunk of the row (128
+// bytes, or 64 when a row is 64 bytes), 1 head, 128 rows, 1 batch}, matching
+// swizzle, zero fill out of bounds (ragged sequence tails).
+bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int D, int H, int S, int B,
+              const Strides& st)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
@@ -161,8 +249,8 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
     const int row_bytes = D * elem_bytes;
     const int swz = row_bytes < 128 ? row_bytes : 128;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)D * elem_bytes, (cuuint64_t)H * D * elem_bytes,
-                                   (cuuint64_t)S * H * D * elem_bytes};
+    const cuuint64_t strides[3] = {(cuuint64_t)st.h * elem_bytes, (cuuint64_t)st.s * elem_bytes,
+                                   (cuuint64_t)st.b * elem_bytes};
     const cuuint32_t box[4] = {(cuuint32_t)(swz / elem_bytes), 1, (cuuint32_t)sdpa::kBlockM, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -181,10 +269,15 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
     return cudaGetLastError();
 }
 
-sdpa::Params make_params(void* O, const Shape& s, double score_scale, float out_scale, int causal)
+sdpa::Params make_params(const Args& a, double score_scale, float out_scale, int causal)
 {
+    const Shape& s = a.s;
     sdpa::Params p{};
-    p.O = O;
+    p.O = a.O;
+    p.o_sb = a.o.b;
+    p.o_ss = a.o.s;
+    p.o_sh = a.o.h;
+    p.lse = a.lse;
     p.B = s.B;
     p.Hq = s.Hq;
     p.Hkv = s.Hkv;
@@ -208,6 +301,64 @@ cudaError_t launch_kind(int D, const CUtensorMap& tq, const CUtensorMap& tk, con
                    : launch<128, KIND>(tq, tk, tv, p, sm_count, stream);
 }
 
+// The forward pass for already resolved arguments: checks, tensor maps,
+// launch.  `descales` is null for 16-bit kinds.
+sdpa_status_t run(const Args& a, float scale, const float* descales, int causal, sdpa_dtype_t dtype,
+                  void* stream)
+{
+    const bool fp8 = dtype == SDPA_DTYPE_E4M3;
+    const int in_bytes = fp8 ? 1 : 2;
+    sdpa_status_t st = check_common(a, in_bytes, 2);
+    if (st != SDPA_OK)
+        return st;
+    if (!valid_scale(scale))
+        return SDPA_ERR_SCALE;
+    double score_scale = scale;
+    float out_scale = 1.f;
+    if (fp8) {
+        if (!valid_scale(descales[0]) || !valid_scale(descales[1]) || !valid_scale(descales[2]))
+            return SDPA_ERR_SCALE;
+        // the folded score scale must stay a finite, positive float
+        score_scale = static_cast<double>(scale) * descales[0] * descales[1];
+        const float c = static_cast<float>(score_scale * 1.4426950408889634);
+        if (!(score_scale > 0.0) || !std::isfinite(c) || c == 0.f)
+            return SDPA_ERR_SCALE;
+        out_scale = descales[2];
+    }
+
+    int dev = 0, sm_count = 0;
+    st = device_ready(&dev, &sm_count);
+    if (st != SDPA_OK)
+        return st;
+
+    const Shape& s = a.s;
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : dtype == SDPA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, a.Q, dt, in_bytes, s.D, s.Hq, s.Sq, s.B, a.q) ||
+        !make_map(&tk, a.K, dt, in_bytes, s.D, s.Hkv, s.Skv, s.B, a.k) ||
+        !make_map(&tv, a.V, dt, in_bytes, s.D, s.Hkv, s.Skv, s.B, a.v))
+        return cuda_fail(cudaErrorInvalidValue);
+
+    const sdpa::Params p = make_params(a, score_scale, out_scale, causal);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = fp8 ? launch_kind<sdpa::kE4M3>(s.D, tq, tk, tv, p, sm_count, cs)
+                        : dtype == SDPA_DTYPE_BF16 ? launch_kind<sdpa::kBF16>(s.D, tq, tk, tv, p, sm_count, cs)
+                                                   : launch_kind<sdpa::kFP16>(s.D, tq, tk, tv, p, sm_count, cs);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    return SDPA_OK;
+}
+
+Args make_args(const void* Q, const void* K, const void* V, void* O, float* lse, int B, int Hq, int Hkv, int Sq,
+               int Skv, int D, const sdpa_layout_t* ql, const sdpa_layout_t* kl, const sdpa_layout_t* vl,
+               const sdpa_layout_t* ol)
+{
+    return Args{Q, K, V, O, lse, Shape{B, Hq, Hkv, Sq, Skv, D},
+                resolve(ql, Sq, Hq, D), resolve(kl, Skv, Hkv, D), resolve(vl, Skv, Hkv, D), resolve(ol, Sq, Hq, D)};
+}
+
 }  // namespace
 
 extern "C" {
@@ -215,68 +366,38 @@ extern "C" {
 sdpa_status_t sdpa_fwd(const void* Q, const void* K, const void* V, void* O, int B, int Hq, int Hkv, int Sq,
                        int Skv, int D, float scale, int causal, sdpa_dtype_t dtype, void* stream)
 {
+    return sdpa_fwd_ex(Q, K, V, O, nullptr, B, Hq, Hkv, Sq, Skv, D, nullptr, nullptr, nullptr, nullptr, scale,
+                       causal, dtype, stream);
+}
+
+sdpa_status_t sdpa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq, int Hkv,
+                          int Sq, int Skv, int D, const sdpa_layout_t* q_layout, const sdpa_layout_t* k_layout,
+                          const sdpa_layout_t* v_layout, const sdpa_layout_t* o_layout, float scale, int causal,
+                          sdpa_dtype_t dtype, void* stream)
+{
     if (dtype != SDPA_DTYPE_BF16 && dtype != SDPA_DTYPE_FP16)
         return SDPA_ERR_DTYPE;
-    const Shape s{B, Hq, Hkv, Sq, Skv, D};
-    sdpa_status_t st = check_common(Q, K, V, O, s, 2, 2);
-    if (st != SDPA_OK)
-        return st;
-    if (!valid_scale(scale))
-        return SDPA_ERR_SCALE;
-
-    int dev = 0, sm_count = 0;
-    st = device_ready(&dev, &sm_count);
-    if (st != SDPA_OK)
-        return st;
-
-    const CUtensorMapDataType dt =
-        dtype == SDPA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, Q, dt, 2, D, Hq, Sq, B) || !make_map(&tk, K, dt, 2, D, Hkv, Skv, B) ||
-        !make_map(&tv, V, dt, 2, D, Hkv, Skv, B))
-        return cuda_fail(cudaErrorInvalidValue);
-
-    const sdpa::Params p = make_params(O, s, scale, 1.f, causal);
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = dtype == SDPA_DTYPE_BF16 ? launch_kind<sdpa::kBF16>(D, tq, tk, tv, p, sm_count, cs)
-                                                   : launch_kind<sdpa::kFP16>(D, tq, tk, tv, p, sm_count, cs);
-    if (e != cudaSuccess)
-        return cuda_fail(e);
-    return SDPA_OK;
+    const Args a = make_args(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, q_layout, k_layout, v_layout, o_layout);
+    return run(a, scale, nullptr, causal, dtype, stream);
 }
 
 sdpa_status_t sdpa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, int B, int Hq, int Hkv, int Sq,
                            int Skv, int D, float scale, float descale_q, float descale_k, float descale_v,
                            int causal, void* stream)
 {
-    const Shape s{B, Hq, Hkv, Sq, Skv, D};
-    sdpa_status_t st = check_common(Q, K, V, O, s, 1, 2);
-    if (st != SDPA_OK)
-        return st;
-    if (!valid_scale(scale) || !valid_scale(descale_q) || !valid_scale(descale_k) || !valid_scale(descale_v))
-        return SDPA_ERR_SCALE;
-    // the folded score scale must stay a finite, positive float
-    const double score_scale = static_cast<double>(scale) * descale_q * descale_k;
-    if (!(score_scale > 0.0) || !std::isfinite(static_cast<float>(score_scale * 1.4426950408889634)) ||
-        static_cast<float>(score_scale * 1.4426950408889634) == 0.f)
-        return SDPA_ERR_SCALE;
+    return sdpa_fwd_fp8_ex(Q, K, V, O, nullptr, B, Hq, Hkv, Sq, Skv, D, nullptr, nullptr, nullptr, nullptr, scale,
+                           descale_q, descale_k, descale_v, causal, stream);
+}
 
-    int dev = 0, sm_count = 0;
-    st = device_ready(&dev, &sm_count);
-    if (st != SDPA_OK)
-        return st;
-
-    CUtensorMap tq, tk, tv;
-    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    if (!make_map(&tq, Q, dt, 1, D, Hq, Sq, B) || !make_map(&tk, K, dt, 1, D, Hkv, Skv, B) ||
-        !make_map(&tv, V, dt, 1, D, Hkv, Skv, B))
-        return cuda_fail(cudaErrorInvalidValue);
-
-    const sdpa::Params p = make_params(O, s, score_scale, descale_v, causal);
-    const cudaError_t e = launch_kind<sdpa::kE4M3>(D, tq, tk, tv, p, sm_count, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess)
-        return cuda_fail(e);
-    return SDPA_OK;
+sdpa_status_t sdpa_fwd_fp8_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
+                              int Hkv, int Sq, int Skv, int D, const sdpa_layout_t* q_layout,
+                              const sdpa_layout_t* k_layout, const sdpa_layout_t* v_layout,
+                              const sdpa_layout_t* o_layout, float scale, float descale_q, float descale_k,
+                              float descale_v, int causal, void* stream)
+{
+    const Args a = make_args(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, q_layout, k_layout, v_layout, o_layout);
+    const float descales[3] = {descale_q, descale_k, descale_v};
+    return run(a, scale, descales, causal, SDPA_DTYPE_E4M3, stream);
 }
 
 const char* sdpa_status_string(sdpa_status_t status)
@@ -293,6 +414,7 @@ const char* sdpa_status_string(sdpa_status_t status)
     case SDPA_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
     case SDPA_ERR_ALIAS: return "output overlaps an input";
     case SDPA_ERR_CUDA: return "CUDA error";
+    case SDPA_ERR_LAYOUT: return "unusable strides";
     }
     return "unknown status";
 }
@@ -323,7 +445,7 @@ sdpa_status_t sdpa_device_error(unsigned int* code)
 
 int sdpa_abi_version(void)
 {
-    return 1;
+    return 2;
 }
 
 }  // extern "C"

@@ -65,6 +65,7 @@ constexpr float kRescaleThreshold = 8.0f;          // log2 units: rescale O when
 // P * 56 <= 2^3 * 56 = 448, the largest finite E4M3 value.
 constexpr float kRescaleThresholdFP8 = 3.0f;
 constexpr float kLog2P8Scale = 5.807354922057604f;  // log2(56)
+constexpr float kLn2 = 0.6931471805599453f;
 
 // Device error word: 0 = no error; otherwise the first failure recorded by any
 // CTA (see the codes below).  Read and cleared by the host through the C-ABI.
@@ -78,6 +79,8 @@ enum : unsigned int {
 
 struct Params {
     void* O;
+    long long o_sb, o_ss, o_sh;      // O strides in elements (batch, sequence, head); D is contiguous
+    float* lse;                      // [B][Hq][Sq] log-sum-exp of each row's scores, or null
     int B, Hq, Hkv, Sq, Skv;
     int group;                       // Hq / Hkv
     int n_units;                     // B * Hq * n_pairs
@@ -748,8 +751,16 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_arrive(smem_u32(&bars->o_empty[t]));
             if (q_idx < p.Sq) {
                 const float inv_l = p.out_scale / l;
+                if (p.lse) {
+                    // log sum_j exp(s_j) = ln 2 * (m + log2 l): m is the max of
+                    // s * log2(e) the weights were taken against, l their sum
+                    // (E4M3: of the weights times 56)
+                    const float lg = kFP8 ? log2f(l) - kLog2P8Scale : log2f(l);
+                    p.lse[((int64_t)w.b * p.Hq + w.hq) * p.Sq + q_idx] = (m + lg) * kLn2;
+                }
                 uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.O) +
-                                                      (((int64_t)w.b * p.Sq + q_idx) * p.Hq + w.hq) * (int64_t)(D * 2));
+                                                      ((int64_t)w.b * p.o_sb + (int64_t)q_idx * p.o_ss +
+                                                       (int64_t)w.hq * p.o_sh) * 2);
 #pragma unroll
                 for (int v = 0; v < D / 8; ++v)
                     dst[v] = make_uint4(pack2<kOutBF16>(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),

@@ -41,7 +41,7 @@ def test_exports_every_declared_function(lib):
 
 def test_abi_version_and_strings(lib):
     assert lib.sdpa_abi_version() >= 1
-    for code in range(11):
+    for code in range(12):
         s = lib.sdpa_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.sdpa_status_string(99).decode() == "unknown status"
@@ -93,3 +93,55 @@ def test_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 128, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         sdpa_fwd(q, q, q)
+
+
+# ------------------------------------------------------------- *_ex checks --
+
+def call_ex(lib, q=QP, k=KP, v=VP, o=OP, lse=None, ql=None, kl=None, vl=None, ol=None, **kw):
+    a = dict(GOOD, **kw)
+    ref = lambda l: ctypes.byref(_abi.Layout(*l)) if l is not None else None
+    return lib.sdpa_fwd_ex(q, k, v, o, lse, a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Skv"], a["D"],
+                           ref(ql), ref(kl), ref(vl), ref(ol), ctypes.c_float(a["scale"]), a["causal"],
+                           a["dtype"], None)
+
+
+D_, SQ, HQ, HKV = 128, 300, 8, 2
+BSHD_Q = (SQ * HQ * D_, HQ * D_, D_)
+BHSD_Q = (HQ * SQ * D_, D_, SQ * D_)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(ql=(BSHD_Q[0], BSHD_Q[1], 4)), 11),           # head stride of 8 bytes: not a multiple of 16
+    (dict(kl=(0, HKV * D_, D_)), 11),                     # zero stride
+    (dict(vl=(-1, HKV * D_, D_)), 11),                    # negative stride
+    (dict(ql=(1 << 40, HQ * D_, D_)), 11),                # 2^41 bytes
+    (dict(ol=(SQ * HQ * D_, D_, D_)), 11),                # O rows overlap: seq and head stride both D
+    (dict(ol=(D_, HQ * D_, D_ * 2)), 11),                 # O batch entries overlap other rows
+    (dict(lse=0x50000002), 2),                            # LSE not 4-byte aligned
+    (dict(lse=OP + 4096), 9),                             # LSE inside O
+    (dict(lse=QP), 9),                                    # LSE inside Q
+    (dict(o=QP + 2 * (HQ * SQ * D_ * 2) - 64, ql=BHSD_Q), 9),   # O starts inside the BHSD span of Q
+    (dict(dtype=2), 6),
+    (dict(q=None), 1),
+])
+def test_ex_rejects_before_any_cuda_call(lib, kw, status):
+    assert call_ex(lib, **kw) == status
+
+
+def test_ex_contiguous_layout_is_the_default(lib):
+    # explicit contiguous strides pass the same checks as NULL layouts: the
+    # only failure left is the device (none here) or a CUDA error
+    st_null = call_ex(lib)
+    st_expl = call_ex(lib, ql=BSHD_Q, kl=(SQ * HKV * D_, HKV * D_, D_), vl=(SQ * HKV * D_, HKV * D_, D_),
+                      ol=BSHD_Q)
+    assert st_null == st_expl and st_null in (8, 10)
+
+
+def test_fp8_ex_checks(lib):
+    f = lib.sdpa_fwd_fp8_ex
+    s = ctypes.c_float
+    bad = ctypes.byref(_abi.Layout(128 * 2 * 64, 2 * 64, 8))    # 8-byte head stride
+    assert f(QP, KP, VP, OP, None, 1, 2, 2, 128, 128, 64, bad, None, None, None,
+             s(0.125), s(1), s(1), s(1), 0, None) == 11
+    assert f(QP, KP, VP, OP, None, 1, 2, 2, 128, 128, 64, None, None, None, None,
+             s(0.125), s(1), s(-1), s(1), 0, None) == 7
