@@ -39,6 +39,12 @@ WORKLOADS = {
     "mha-causal-1024": (4, 16, 16, 1024, 64, True, "bf16"),
     "fp8-causal-8192": (2, 16, 16, 8192, 128, True, "e4m3"),
 }
+# the codelab's small timing problem (B=4, T=128, N=8) at D = 32 / 64 / 128 and
+# its batch sweep at T=256: launch-latency rows
+for _D in (32, 64, 128):
+    WORKLOADS[f"latency-b4-t128-d{_D}"] = (4, 8, 8, 128, _D, False, "bf16")
+for _B in (1, 2, 4, 8, 16):
+    WORKLOADS[f"batch-{_B}-t256"] = (_B, 8, 8, 256, 64, False, "bf16")
 for _B, _S in [(64, 512), (32, 1024), (16, 2048), (8, 4096), (4, 8192), (2, 16384)]:
     WORKLOADS[f"mqa-causal-{_S}"] = (_B, 32, 1, _S, 128, True, "bf16")
     WORKLOADS[f"mqa-full-{_S}"] = (_B, 32, 1, _S, 128, False, "bf16")

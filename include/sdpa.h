@@ -57,7 +57,7 @@ typedef enum {
     SDPA_ERR_MISALIGNED = 2,   /* a pointer is not 16-byte aligned */
     SDPA_ERR_BAD_SHAPE = 3,    /* a size is < 1 or too large */
     SDPA_ERR_HEADS = 4,        /* Hq is not a multiple of Hkv */
-    SDPA_ERR_HEAD_DIM = 5,     /* D is not 64 or 128 */
+    SDPA_ERR_HEAD_DIM = 5,     /* D is not 32, 64 or 128 (E4M3: 64 or 128) */
     SDPA_ERR_DTYPE = 6,        /* unknown dtype, or E4M3 passed to sdpa_fwd */
     SDPA_ERR_SCALE = 7,        /* scale (or a descale) is not finite and > 0 */
     SDPA_ERR_ARCH = 8,         /* current device is not compute capability 10.3 */
@@ -89,7 +89,8 @@ typedef struct {
  *   O         device, written, [B][Sq][Hq][D], element type `dtype`; must not
  *             overlap Q, K or V.
  *   B, Hq, Hkv, Sq, Skv   >= 1, Hq % Hkv == 0.
- *   D         64 or 128.
+ *   D         32, 64 or 128 (section 12, "Next steps", suggests trying 32,
+ *             64 and 128).
  *   scale     finite, > 0; section 4 ("Implement attention from scratch")
  *             uses 1/sqrt(D).
  *   causal    0 = no mask, nonzero = lower-triangular mask.

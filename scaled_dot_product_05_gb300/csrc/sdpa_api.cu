@@ -87,7 +87,8 @@ sdpa_status_t device_ready(int* dev_out, int* sm_count)
             st.err = e3;
             return;
         }
-        cudaError_t es[] = {set_attrs<64, sdpa::kBF16>(),  set_attrs<64, sdpa::kFP16>(),
+        cudaError_t es[] = {set_attrs<32, sdpa::kBF16>(),  set_attrs<32, sdpa::kFP16>(),
+                            set_attrs<64, sdpa::kBF16>(),  set_attrs<64, sdpa::kFP16>(),
                             set_attrs<64, sdpa::kE4M3>(),  set_attrs<128, sdpa::kBF16>(),
                             set_attrs<128, sdpa::kFP16>(), set_attrs<128, sdpa::kE4M3>()};
         for (cudaError_t x : es)
@@ -204,7 +205,8 @@ sdpa_status_t check_common(const Args& a, int in_elem_bytes, int out_elem_bytes)
         return SDPA_ERR_BAD_SHAPE;
     if (s.Hq % s.Hkv != 0)
         return SDPA_ERR_HEADS;
-    if (s.D != 64 && s.D != 128)
+    // D = 32 only for 16-bit elements: E4M3 rows would be 32 bytes
+    if (s.D != 64 && s.D != 128 && !(s.D == 32 && in_elem_bytes == 2))
         return SDPA_ERR_HEAD_DIM;
     // the B * Hq * ceil(Sq / 256) work units are counted in int
     const int64_t n_pairs = (static_cast<int64_t>(s.Sq) + sdpa::kUnitRows - 1) / sdpa::kUnitRows;
@@ -297,6 +299,11 @@ template <int KIND>
 cudaError_t launch_kind(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const sdpa::Params& p, int sm_count, cudaStream_t stream)
 {
+    if (D == 32) {
+        if constexpr (KIND != sdpa::kE4M3)
+            return launch<32, KIND>(tq, tk, tv, p, sm_count, stream);
+        return cudaErrorInvalidValue;           // rejected by check_common
+    }
     return D == 64 ? launch<64, KIND>(tq, tk, tv, p, sm_count, stream)
                    : launch<128, KIND>(tq, tk, tv, p, sm_count, stream);
 }

@@ -100,6 +100,8 @@ enum Kind : int { kBF16 = 0, kFP16 = 1, kE4M3 = 2 };
 // (128-byte, or 64-byte when a row holds only 64 bytes).
 template <int D, int KIND>
 struct Layout {
+    static_assert(D == 32 || D == 64 || D == 128, "head dimension");
+    static_assert(D != 32 || KIND != kE4M3, "E4M3 needs rows of at least 64 bytes");
     static constexpr int kEsize = (KIND == kE4M3) ? 1 : 2;
     static constexpr int kRowBytes = D * kEsize;
     static constexpr int kSwz = kRowBytes < 128 ? kRowBytes : 128;     // swizzle span in bytes
@@ -742,8 +744,9 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if constexpr (D == 128) {
                 tmem_ld128_wait(o_tmem, o_tmem + 32, o_tmem + 64, o_tmem + 96, o);
             } else {
-                tmem_ld32_wait(o_tmem, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-                tmem_ld32_wait(o_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc)
+                    tmem_ld32_wait(o_tmem + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&o[32 * cc]));
             }
             if constexpr (kFP8)
                 l = __uint_as_float(tmem_ld1_wait(l_tmem));   // sum of the E4M3 P values (tensor core, fp32)

@@ -64,7 +64,7 @@ def call(lib, q=QP, k=KP, v=VP, o=OP, **kw):
     (dict(B=0), 3), (dict(Hq=0), 3), (dict(Hkv=0), 3), (dict(Sq=0), 3), (dict(Skv=0), 3), (dict(Sq=-5), 3),
     (dict(B=1 << 20, Hq=1 << 12), 3),
     (dict(Hq=6, Hkv=4), 4),
-    (dict(D=32), 5), (dict(D=96), 5), (dict(D=256), 5),
+    (dict(D=16), 5), (dict(D=96), 5), (dict(D=256), 5), (dict(D=0), 5),
     (dict(dtype=2), 6), (dict(dtype=7), 6),
     (dict(scale=0.0), 7), (dict(scale=-1.0), 7), (dict(scale=float("inf")), 7), (dict(scale=float("nan")), 7),
     (dict(o=QP + 16), 9), (dict(o=VP - 64), 9),
@@ -78,6 +78,8 @@ def test_fp8_entry_checks(lib):
     s = ctypes.c_float
     assert f(QP, KP, VP, None, 1, 2, 2, 128, 128, 64, s(0.125), s(1), s(1), s(1), 0, None) == 1
     assert f(QP, KP, VP, OP, 1, 2, 2, 128, 128, 64, s(0.125), s(0.0), s(1), s(1), 0, None) == 7
+    # E4M3 rows must hold at least 64 bytes: D = 32 is a 16-bit-only head size
+    assert f(QP, KP, VP, OP, 1, 2, 2, 128, 128, 32, s(0.125), s(1), s(1), s(1), 0, None) == 5
     assert f(QP, KP, VP, OP, 1, 2, 2, 128, 128, 48, s(0.125), s(1), s(1), s(1), 0, None) == 5
 
 

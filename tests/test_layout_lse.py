@@ -92,7 +92,7 @@ def check_lse(lse, ref_lse, dtype, what):
     assert err <= LSE_TOL[dtype], f"{what}: LSE max_abs {err:.3e} > {LSE_TOL[dtype]}"
 
 
-SHAPES = [(2, 4, 2, 300, 300, 128), (1, 4, 4, 200, 77, 64), (1, 8, 1, 129, 400, 128)]
+SHAPES = [(2, 4, 2, 300, 300, 128), (1, 4, 4, 200, 77, 64), (1, 8, 1, 129, 400, 128), (1, 4, 2, 260, 260, 32)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))

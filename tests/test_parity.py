@@ -50,6 +50,8 @@ SMALL = [
     (1, 2, 1, 1, 500, 64),
     (1, 2, 2, 500, 1, 128),
     (1, 6, 3, 640, 640, 128),
+    (2, 4, 2, 300, 300, 32),
+    (1, 8, 8, 129, 520, 32),
 ]
 
 
@@ -132,6 +134,25 @@ def test_causal_mha_1024_full():
     o = run_gpu(x, True)
     ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=True, dtype="bf16")
     assert_close(to_np(o), ref, "bf16", "causal MHA S=1024")
+
+
+@pytest.mark.parametrize("D", [32, 64, 128])
+def test_latency_row_b4_t128_full(D):
+    # the codelab's small timing problem (B=4, T=128, N=8 heads, section 8),
+    # with the head sizes its "Next steps" suggest; non-causal
+    x = make_qkv(7 + D, 4, 8, 8, 128, 128, D, "bf16")
+    o = run_gpu(x, False)
+    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=False, dtype="bf16")
+    assert_close(to_np(o), ref, "bf16", f"b4 t128 d{D}")
+
+
+@pytest.mark.parametrize("B", [1, 16])
+def test_batch_sweep_t256_full(B):
+    # the batch sweep at T=256 (section 8): smallest and largest batch
+    x = make_qkv(100 + B, B, 8, 8, 256, 256, 64, "bf16")
+    o = run_gpu(x, False)
+    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=False, dtype="bf16")
+    assert_close(to_np(o), ref, "bf16", f"batch {B}")
 
 
 def test_causal_gqa_4096_sampled():
