@@ -69,6 +69,12 @@ def step_bytes(name):
     return B * S * D * (Hq * e_in + 2 * Hkv * e_in + Hq * 2)
 
 
+def n_rotating_sets(name):
+    """Input sets to rotate through so that together they hold at least twice
+    L2 (two at the least)."""
+    return int(min(4096, max(2, -(-2 * L2_BYTES // step_bytes(name)))))
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "scaled_dot_product_05_gb300", "csrc")
@@ -262,8 +268,10 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
 
-    # two resident input sets (different seeds) used alternately, so a step
-    # never finds its inputs in L2 from the previous step
+    # resident input sets used in rotation, enough that together they hold at
+    # least twice L2, so a step never finds its inputs in L2 from an earlier
+    # step: two seeded sets, the rest device copies of them
+    n_sets = n_rotating_sets(name)
     sets = []
     host = None
     for s in range(2):
@@ -273,14 +281,18 @@ def run_gpu(args, rank, world, local_rank):
         sets.append((q, k, v, o, x.descales))
         if s == 0:
             host = x
+    for s in range(2, n_sets):
+        q, k, v, o, ds = sets[s & 1]
+        sets.append((q.clone(), k.clone(), v.clone(), torch.empty_like(o), ds))
 
-    def launch(i, tensors=None):
-        q, k, v, o, ds = tensors if tensors is not None else sets[i & 1]
+    def launch(i, tensors=None, on=None):
+        q, k, v, o, ds = tensors if tensors is not None else sets[i % n_sets]
+        st = on if on is not None else stream
         if dtype == "e4m3":
             sdpa_fwd_fp8(q, k, v, o, descale_q=ds[0], descale_k=ds[1], descale_v=ds[2], causal=causal,
-                         stream=stream)
+                         stream=st)
         else:
-            sdpa_fwd(q, k, v, o, causal=causal, stream=stream)
+            sdpa_fwd(q, k, v, o, causal=causal, stream=st)
 
     def barrier():
         if world > 1:
@@ -296,20 +308,45 @@ def run_gpu(args, rank, world, local_rank):
         time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # timed region 1: the K steps back to back, as a caller issues them
     barrier()
     t_wall0 = time.time()
     start.record(stream)
     for i in range(args.steps):
+        launch(i)
+    end.record(stream)
+    barrier()
+    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_per_step = total_ms / args.steps
+    # timed region 2: the same K steps, each bracketed by its own events on
+    # the launching stream (the kernel's launch duration for the roofline)
+    for i in range(args.steps):
         ev[i][0].record(stream)
         launch(i)
         ev[i][1].record(stream)
-    end.record(stream)
     barrier()
     t_wall1 = time.time()
-    total_ms = start.elapsed_time(end)
     kern_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = max_over_ranks(total_ms, world, dev)
-    ms_per_step = total_ms / args.steps
+    # the same launches captured in one CUDA graph and replayed: launch
+    # latency without the Python call (what a graph-capturing caller sees)
+    g_launches = min(args.steps, 32)
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for i in range(g_launches):
+            launch(i, on=cap)
+    graph.replay()
+    barrier()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(3):
+        graph.replay()
+    g1.record(stream)
+    barrier()
+    graph_ms = g0.elapsed_time(g1) / (3 * g_launches)
+    del graph
     err = sdpa_device_error()
     if err:
         raise RuntimeError(f"device error word 0x{err:x}")
@@ -425,14 +462,19 @@ def run_gpu(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded N(0,1), inputs resident in HBM)",
         "config": {"workload": describe(name), "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": S, "Skv": S, "D": D,
                    "causal": causal, "flops_per_step": flops, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2 ({step_bytes(name) / 1e6:.1f} MB per step, 2 rotating sets)"},
+                   "l2": f"inputs larger than L2 ({n_sets} rotating input sets of {step_bytes(name) / 1e6:.1f} MB, "
+                         f"{n_sets * step_bytes(name) / 1e6:.0f} MB in all)"},
         "roofline": roofline,
         "e2e": {"value": whole_job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
                 "pipelined": "H2D / kernel / D2H on three streams over two device buffer sets",
                 "serial_ms_per_step": e2e_serial_ms,
                 "serial_value": whole_job_tflops(flops, world, e2e_serial_ms)},
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,
+        "graph": {"ms_per_launch": graph_ms, "launches": 3 * g_launches,
+                  "note": "the same launches captured in one CUDA graph and replayed (no Python call per launch); "
+                          "timed regions 1 (back to back, gives value) and 2 (per-launch events, gives the "
+                          "roofline's launch duration) hold K launches each"},
         "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
     }
     if not args.no_cpu_baseline:

@@ -20,9 +20,16 @@ __all__ = ["sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_s
 _DTYPE = {torch.bfloat16: _abi.SDPA_DTYPE_BF16, torch.float16: _abi.SDPA_DTYPE_FP16}
 
 
-def _stream_ptr(stream):
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_ptr(stream, device_index: int):
+    """cudaStream_t for the call: the given stream, else the current stream
+    of the tensors' device (read without building a Stream object)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        if _raw_stream is not None:
+            return ctypes.c_void_p(_raw_stream(device_index))
+        stream = torch.cuda.current_stream(device_index)
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
@@ -56,7 +63,7 @@ def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor 
         scale = 1.0 / math.sqrt(D)
     dt = _DTYPE.get(q.dtype, 99)
     check(lib().sdpa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
-                         float(scale), int(bool(causal)), dt, _stream_ptr(stream)))
+                         float(scale), int(bool(causal)), dt, _stream_ptr(stream, q.device.index)))
     return o
 
 
@@ -77,7 +84,7 @@ def sdpa_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Ten
         scale = 1.0 / math.sqrt(D)
     check(lib().sdpa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
                              float(scale), float(descale_q), float(descale_k), float(descale_v),
-                             int(bool(causal)), _stream_ptr(stream)))
+                             int(bool(causal)), _stream_ptr(stream, q.device.index)))
     return o
 
 
@@ -116,7 +123,7 @@ def sdpa_fwd_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tens
     check(lib().sdpa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _lse_ptr(lse, B, Hq, Sq),
                             B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq), ctypes.byref(lk), ctypes.byref(lv),
                             ctypes.byref(lo), float(scale), int(bool(causal)), _DTYPE.get(q.dtype, 99),
-                            _stream_ptr(stream)))
+                            _stream_ptr(stream, q.device.index)))
     return o
 
 
@@ -138,7 +145,7 @@ def sdpa_fwd_fp8_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.
     check(lib().sdpa_fwd_fp8_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _lse_ptr(lse, B, Hq, Sq),
                                 B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq), ctypes.byref(lk), ctypes.byref(lv),
                                 ctypes.byref(lo), float(scale), float(descale_q), float(descale_k),
-                                float(descale_v), int(bool(causal)), _stream_ptr(stream)))
+                                float(descale_v), int(bool(causal)), _stream_ptr(stream, q.device.index)))
     return o
 
 

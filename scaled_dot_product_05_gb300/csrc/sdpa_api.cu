@@ -242,8 +242,8 @@ bool valid_scale(float x)
 // (innermost first) {D, H, S, B}, box {one swizzle chunk of the row (128
 // bytes, or 64 when a row is 64 bytes), 1 head, 128 rows, 1 batch}, matching
 // swizzle, zero fill out of bounds (ragged sequence tails).
-bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int D, int H, int S, int B,
-              const Strides& st)
+bool encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int D, int H, int S, int B,
+                const Strides& st)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
@@ -258,6 +258,56 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
     return enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A tensor map depends only on these fields, so an encoded map can be reused
+// whenever they repeat (repeated calls on the same buffers): a small
+// per-thread cache, replaced round robin, saves the host-side encoding.
+struct MapKey {
+    const void* base;
+    long long sb, ss, sh;
+    int dt, elem_bytes, D, H, S, B;
+};
+
+struct MapCache {
+    static constexpr int kSize = 12;
+    MapKey key[kSize];
+    CUtensorMap map[kSize];
+    bool used[kSize] = {};
+    int next = 0;
+};
+
+thread_local MapCache t_maps;
+
+bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int D, int H, int S, int B,
+              const Strides& st)
+{
+    MapKey k;
+    std::memset(&k, 0, sizeof k);                    // padding bytes take part in the comparison
+    k.base = base;
+    k.sb = st.b;
+    k.ss = st.s;
+    k.sh = st.h;
+    k.dt = static_cast<int>(dt);
+    k.elem_bytes = elem_bytes;
+    k.D = D;
+    k.H = H;
+    k.S = S;
+    k.B = B;
+    MapCache& c = t_maps;
+    for (int i = 0; i < MapCache::kSize; ++i)
+        if (c.used[i] && std::memcmp(&c.key[i], &k, sizeof k) == 0) {
+            *map = c.map[i];
+            return true;
+        }
+    if (!encode_map(map, base, dt, elem_bytes, D, H, S, B, st))
+        return false;
+    const int slot = c.next;
+    c.next = (c.next + 1) % MapCache::kSize;
+    std::memcpy(&c.key[slot], &k, sizeof k);
+    c.map[slot] = *map;
+    c.used[slot] = true;
+    return true;
 }
 
 template <int D, int KIND>

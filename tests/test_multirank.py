@@ -43,3 +43,12 @@ def test_single_rank_passthrough():
     import bench
     assert bench.max_over_ranks(1.25, 1, torch.device("cpu")) == 1.25
     assert bench.whole_job_tflops(2e12, 1, 1.0) == pytest.approx(2000.0)
+
+
+def test_rotating_sets_exceed_l2():
+    # every workload rotates through input sets that together hold >= 2 x L2
+    import bench
+    for name in bench.WORKLOADS:
+        n = bench.n_rotating_sets(name)
+        assert n >= 2
+        assert n * bench.step_bytes(name) >= 2 * bench.L2_BYTES or n == 4096
