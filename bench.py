@@ -48,25 +48,54 @@ for _B in (1, 2, 4, 8, 16):
 for _B, _S in [(64, 512), (32, 1024), (16, 2048), (8, 4096), (4, 8192), (2, 16384)]:
     WORKLOADS[f"mqa-causal-{_S}"] = (_B, 32, 1, _S, 128, True, "bf16")
     WORKLOADS[f"mqa-full-{_S}"] = (_B, 32, 1, _S, 128, False, "bf16")
+# decode shapes (few query rows, long K/V; non-causal), run through the
+# decode pass with a split workspace: name -> (B, Hq, Hkv, Sq, Skv, D)
+DECODE_WORKLOADS = {
+    "decode-gqa-b8-32k": (8, 32, 8, 1, 32768, 128),
+    "decode-gqa-b32-8k": (32, 32, 8, 4, 8192, 128),
+}
 DEFAULT_WORKLOAD = "gqa-causal-4096"
 
 
-def describe(name):
+class Spec(tuple):
+    """(B, Hq, Hkv, Sq, Skv, D, causal, dtype, decode) of a workload."""
+    __slots__ = ()
+    B = property(lambda t: t[0]); Hq = property(lambda t: t[1]); Hkv = property(lambda t: t[2])
+    Sq = property(lambda t: t[3]); Skv = property(lambda t: t[4]); D = property(lambda t: t[5])
+    causal = property(lambda t: t[6]); dtype = property(lambda t: t[7]); decode = property(lambda t: t[8])
+
+
+def spec(name):
+    if name in DECODE_WORKLOADS:
+        B, Hq, Hkv, Sq, Skv, D = DECODE_WORKLOADS[name]
+        return Spec((B, Hq, Hkv, Sq, Skv, D, False, "bf16", True))
     B, Hq, Hkv, S, D, causal, dtype = WORKLOADS[name]
-    return f"{'causal' if causal else 'non-causal'} B={B} Hq={Hq} Hkv={Hkv} Sq=Skv={S} D={D} {dtype}"
+    return Spec((B, Hq, Hkv, S, S, D, causal, dtype, False))
+
+
+ALL_WORKLOADS = sorted(list(WORKLOADS) + list(DECODE_WORKLOADS))
+
+
+def describe(name):
+    w = spec(name)
+    seq = f"Sq=Skv={w.Sq}" if w.Sq == w.Skv else f"Sq={w.Sq} Skv={w.Skv}"
+    kind = "decode pass, " if w.decode else ""
+    return (f"{kind}{'causal' if w.causal else 'non-causal'} B={w.B} Hq={w.Hq} Hkv={w.Hkv} {seq} D={w.D} "
+            f"{w.dtype}")
 
 
 def step_flops(name):
-    B, Hq, Hkv, S, D, causal, _ = WORKLOADS[name]
-    f = 4.0 * B * Hq * S * S * D
-    return f / 2 if causal else f
+    """4 D FLOPs per visible score (causal: the lower triangle, Sq = Skv)."""
+    w = spec(name)
+    f = 4.0 * w.B * w.Hq * w.Sq * w.Skv * w.D
+    return f / 2 if w.causal else f
 
 
 def step_bytes(name):
     """Algorithmic bytes: Q, K, V read once and O written once."""
-    B, Hq, Hkv, S, D, _, dtype = WORKLOADS[name]
-    e_in = 1 if dtype == "e4m3" else 2
-    return B * S * D * (Hq * e_in + 2 * Hkv * e_in + Hq * 2)
+    w = spec(name)
+    e_in = 1 if w.dtype == "e4m3" else 2
+    return w.B * w.D * (w.Sq * w.Hq * e_in + 2 * w.Skv * w.Hkv * e_in + w.Sq * w.Hq * 2)
 
 
 def n_rotating_sets(name):
@@ -193,14 +222,15 @@ def oracle_sample(name, seconds_target=12.0, threads=0):
     import oracle
     from sdpa_inputs import make_qkv
 
-    B, Hq, Hkv, S, D, causal, dtype = WORKLOADS[name]
-    x = make_qkv(1000, B, Hq, Hkv, S, S, D, dtype)
+    w = spec(name)
+    B, Hq, Hkv, Sq, Skv, D, causal, dtype = w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.causal, w.dtype
+    x = make_qkv(1000, B, Hq, Hkv, Sq, Skv, D, dtype)
     rng = np.random.default_rng(1001)
-    total_rows = B * S * Hq
+    total_rows = B * Sq * Hq
 
     def flops_of(rows):
-        i = (np.asarray(rows) // Hq) % S
-        vis = np.minimum(i + 1, S) if causal else np.full(len(rows), S)
+        i = (np.asarray(rows) // Hq) % Sq
+        vis = np.minimum(i + 1, Skv) if causal else np.full(len(rows), Skv)
         return 4.0 * D * float(vis.sum())
 
     def run(rows):
@@ -229,7 +259,6 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     import numpy as np  # noqa: F401
-    B, Hq, Hkv, S, D, causal, dtype = WORKLOADS[name]
     per_step_target = max(1.0, min(20.0, 90.0 / max(1, args.steps + args.warmup)))
     values = []
     desc, cores = "", 0
@@ -259,11 +288,13 @@ def run_gpu(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
 
-    from scaled_dot_product_05_gb300 import sdpa_device_error, sdpa_fwd, sdpa_fwd_fp8
+    from scaled_dot_product_05_gb300 import (decode_workspace_bytes, sdpa_device_error, sdpa_fwd, sdpa_fwd_decode,
+                                             sdpa_fwd_fp8)
     from sdpa_inputs import make_qkv
 
     name = args.workload
-    B, Hq, Hkv, S, D, causal, dtype = WORKLOADS[name]
+    w = spec(name)
+    B, Hq, Hkv, Sq, Skv, D, causal, dtype = w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D, w.causal, w.dtype
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
@@ -275,9 +306,9 @@ def run_gpu(args, rank, world, local_rank):
     sets = []
     host = None
     for s in range(2):
-        x = make_qkv(100 + 17 * rank + s, B, Hq, Hkv, S, S, D, dtype)
+        x = make_qkv(100 + 17 * rank + s, B, Hq, Hkv, Sq, Skv, D, dtype)
         q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
-        o = torch.empty((B, S, Hq, D), dtype=torch.bfloat16 if dtype == "e4m3" else q.dtype, device=dev)
+        o = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16 if dtype == "e4m3" else q.dtype, device=dev)
         sets.append((q, k, v, o, x.descales))
         if s == 0:
             host = x
@@ -285,10 +316,18 @@ def run_gpu(args, rank, world, local_rank):
         q, k, v, o, ds = sets[s & 1]
         sets.append((q.clone(), k.clone(), v.clone(), torch.empty_like(o), ds))
 
+    # decode pass: one split workspace, reused by the launches (they run in
+    # stream order, never at the same time)
+    ws = None
+    if w.decode:
+        ws = torch.empty(max(16, decode_workspace_bytes(B, Hq, Hkv, Sq, Skv, D)), dtype=torch.uint8, device=dev)
+
     def launch(i, tensors=None, on=None):
         q, k, v, o, ds = tensors if tensors is not None else sets[i % n_sets]
         st = on if on is not None else stream
-        if dtype == "e4m3":
+        if w.decode:
+            sdpa_fwd_decode(q, k, v, o, workspace=ws, stream=st)
+        elif dtype == "e4m3":
             sdpa_fwd_fp8(q, k, v, o, descale_q=ds[0], descale_k=ds[1], descale_v=ds[2], causal=causal,
                          stream=st)
         else:
@@ -460,7 +499,7 @@ def run_gpu(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded N(0,1), inputs resident in HBM)",
-        "config": {"workload": describe(name), "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": S, "Skv": S, "D": D,
+        "config": {"workload": describe(name), "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": Sq, "Skv": Skv, "D": D,
                    "causal": causal, "flops_per_step": flops, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({n_sets} rotating input sets of {step_bytes(name) / 1e6:.1f} MB, "
                          f"{n_sets * step_bytes(name) / 1e6:.0f} MB in all)"},
@@ -490,7 +529,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", choices=ALL_WORKLOADS, default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()

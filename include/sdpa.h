@@ -63,7 +63,8 @@ typedef enum {
     SDPA_ERR_ARCH = 8,         /* current device is not compute capability 10.3 */
     SDPA_ERR_ALIAS = 9,        /* O (or LSE) overlaps an input or each other */
     SDPA_ERR_CUDA = 10,        /* a CUDA call failed; see sdpa_last_cuda_error() */
-    SDPA_ERR_LAYOUT = 11       /* a stride is unusable (see sdpa_layout_t) */
+    SDPA_ERR_LAYOUT = 11,      /* a stride is unusable (see sdpa_layout_t) */
+    SDPA_ERR_WORKSPACE = 12    /* workspace too small or not 16-byte aligned */
 } sdpa_status_t;
 
 /*
@@ -153,6 +154,37 @@ sdpa_status_t sdpa_fwd_fp8_ex(const void *Q, const void *K, const void *V, void 
                               float scale, float descale_q, float descale_k, float descale_v,
                               int causal, void *stream);
 
+/*
+ * Decode-shaped forward pass (few query rows against a long key sequence),
+ * non-causal, bf16 or fp16.  Section 9 ("Compare MHA, GQA and MQA") motivates
+ * GQA / MQA by the KV-cache memory of inference; here the G = Hq / Hkv query
+ * heads that read one KV head are stacked into the 128 rows of a query tile
+ * (row s * G + h), so each K/V tile is read once for all G heads, and the key
+ * sequence may be split across units whose results are merged by their
+ * log-sum-exp.
+ *   G         Hq / Hkv must divide 128 (SDPA_ERR_HEADS otherwise).
+ *   workspace device scratch for the split results, at least
+ *             sdpa_decode_workspace_bytes(...) bytes, 16-byte aligned, not
+ *             overlapping Q, K, V, O or LSE; owned by the caller, contents
+ *             need no initialisation, and it must not be used by another
+ *             call running at the same time.  NULL: no split (one unit per
+ *             KV head and group of 256 stacked rows).
+ * Other arguments as for sdpa_fwd_ex (the result is the same attention).
+ */
+sdpa_status_t sdpa_fwd_decode(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                              int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                              const sdpa_layout_t *q_layout, const sdpa_layout_t *k_layout,
+                              const sdpa_layout_t *v_layout, const sdpa_layout_t *o_layout,
+                              float scale, sdpa_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
+ * Workspace bytes sdpa_fwd_decode needs for this shape on the current device
+ * (0: no split, or invalid sizes).  Initialises the library on the current
+ * device on first use.
+ */
+size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int D);
+
 /* Static, human-readable name of a status code. */
 const char *sdpa_status_string(sdpa_status_t status);
 
@@ -167,7 +199,7 @@ int sdpa_last_cuda_error(void);
  */
 sdpa_status_t sdpa_device_error(unsigned int *code);
 
-/* Version of this ABI (bumped on any change; 2 added the *_ex entry points). */
+/* Version of this ABI (bumped on any change; 2 added the *_ex entry points, 3 the decode pass). */
 int sdpa_abi_version(void);
 
 #ifdef __cplusplus

@@ -14,8 +14,8 @@ import torch
 from . import _abi
 from ._abi import SdpaError, check, lib, status_string
 
-__all__ = ["sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_status_string",
-           "sdpa_device_error", "SdpaError", "lib"]
+__all__ = ["sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_fwd_decode",
+           "decode_workspace_bytes", "sdpa_status_string", "sdpa_device_error", "SdpaError", "lib"]
 
 _DTYPE = {torch.bfloat16: _abi.SDPA_DTYPE_BF16, torch.float16: _abi.SDPA_DTYPE_FP16}
 
@@ -146,6 +146,43 @@ def sdpa_fwd_fp8_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.
                                 B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq), ctypes.byref(lk), ctypes.byref(lv),
                                 ctypes.byref(lo), float(scale), float(descale_q), float(descale_k),
                                 float(descale_v), int(bool(causal)), _stream_ptr(stream, q.device.index)))
+    return o
+
+
+def decode_workspace_bytes(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int) -> int:
+    """Workspace bytes sdpa_fwd_decode needs for this shape on the current
+    device (0: the pass is not split)."""
+    return int(lib().sdpa_decode_workspace_bytes(B, Hq, Hkv, Sq, Skv, D))
+
+
+def sdpa_fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                    lse: torch.Tensor | None = None, *, workspace: torch.Tensor | None = None,
+                    scale: float | None = None, stream=None) -> torch.Tensor:
+    """Non-causal decode-shaped pass (few query rows, long K/V): the query
+    heads of each KV head are stacked into one tile, and with ``workspace``
+    (a CUDA tensor of at least :func:`decode_workspace_bytes` bytes) the key
+    sequence is split across the GPU.  Strided views and ``lse`` as for
+    :func:`sdpa_fwd_ex`.  Returns ``o``."""
+    for t in (q, k, v, o):
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+    if q.dtype != k.dtype or q.dtype != v.dtype or o.dtype != q.dtype or tuple(o.shape) != tuple(q.shape):
+        raise ValueError("q, k, v, o must share a dtype; o is shaped like q")
+    B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+    if tuple(k.shape) != tuple(v.shape):
+        raise ValueError("K and V must have the same shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ws, ws_bytes = None, 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    lq, lk, lv, lo = _layout(q), _layout(k), _layout(v), _layout(o)
+    check(lib().sdpa_fwd_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _lse_ptr(lse, B, Hq, Sq),
+                                B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq), ctypes.byref(lk), ctypes.byref(lv),
+                                ctypes.byref(lo), float(scale), _DTYPE.get(q.dtype, 99), ws, ws_bytes,
+                                _stream_ptr(stream, q.device.index)))
     return o
 
 

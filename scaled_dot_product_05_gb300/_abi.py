@@ -10,10 +10,12 @@ from .build import LIB_PATH
 SDPA_DTYPE_BF16, SDPA_DTYPE_FP16, SDPA_DTYPE_E4M3 = 0, 1, 2
 STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_NULL_PTR", 2: "SDPA_ERR_MISALIGNED", 3: "SDPA_ERR_BAD_SHAPE",
           4: "SDPA_ERR_HEADS", 5: "SDPA_ERR_HEAD_DIM", 6: "SDPA_ERR_DTYPE", 7: "SDPA_ERR_SCALE",
-          8: "SDPA_ERR_ARCH", 9: "SDPA_ERR_ALIAS", 10: "SDPA_ERR_CUDA", 11: "SDPA_ERR_LAYOUT"}
+          8: "SDPA_ERR_ARCH", 9: "SDPA_ERR_ALIAS", 10: "SDPA_ERR_CUDA", 11: "SDPA_ERR_LAYOUT",
+          12: "SDPA_ERR_WORKSPACE"}
 # every function include/sdpa.h declares
-EXPORTS = ("sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_status_string",
-           "sdpa_last_cuda_error", "sdpa_device_error", "sdpa_abi_version")
+EXPORTS = ("sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_fwd_decode",
+           "sdpa_decode_workspace_bytes", "sdpa_status_string", "sdpa_last_cuda_error", "sdpa_device_error",
+           "sdpa_abi_version")
 
 
 class Layout(ctypes.Structure):
@@ -42,6 +44,10 @@ def _bind(lib):
     lib.sdpa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, lp, lp, lp, lp, f, i, i, vp]
     lib.sdpa_fwd_fp8_ex.restype = i
     lib.sdpa_fwd_fp8_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, lp, lp, lp, lp, f, f, f, f, i, vp]
+    lib.sdpa_fwd_decode.restype = i
+    lib.sdpa_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, lp, lp, lp, lp, f, i, vp, ctypes.c_size_t, vp]
+    lib.sdpa_decode_workspace_bytes.restype = ctypes.c_size_t
+    lib.sdpa_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
     lib.sdpa_status_string.restype = ctypes.c_char_p
     lib.sdpa_status_string.argtypes = [i]
     lib.sdpa_last_cuda_error.restype = i

@@ -55,10 +55,10 @@ struct DeviceState {
 };
 DeviceState g_dev[kMaxDevices];
 
-template <int D, int KIND>
+template <int D, int KIND, bool kPacked = false>
 cudaError_t set_attrs()
 {
-    return cudaFuncSetAttribute(sdpa::sdpa_fwd_kernel<D, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(sdpa::sdpa_fwd_kernel<D, KIND, kPacked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 sdpa::Layout<D, KIND>::kSmemBytes);
 }
 
@@ -87,10 +87,13 @@ sdpa_status_t device_ready(int* dev_out, int* sm_count)
             st.err = e3;
             return;
         }
-        cudaError_t es[] = {set_attrs<32, sdpa::kBF16>(),  set_attrs<32, sdpa::kFP16>(),
-                            set_attrs<64, sdpa::kBF16>(),  set_attrs<64, sdpa::kFP16>(),
-                            set_attrs<64, sdpa::kE4M3>(),  set_attrs<128, sdpa::kBF16>(),
-                            set_attrs<128, sdpa::kFP16>(), set_attrs<128, sdpa::kE4M3>()};
+        cudaError_t es[] = {set_attrs<32, sdpa::kBF16>(),        set_attrs<32, sdpa::kFP16>(),
+                            set_attrs<64, sdpa::kBF16>(),        set_attrs<64, sdpa::kFP16>(),
+                            set_attrs<64, sdpa::kE4M3>(),        set_attrs<128, sdpa::kBF16>(),
+                            set_attrs<128, sdpa::kFP16>(),       set_attrs<128, sdpa::kE4M3>(),
+                            set_attrs<32, sdpa::kBF16, true>(),  set_attrs<32, sdpa::kFP16, true>(),
+                            set_attrs<64, sdpa::kBF16, true>(),  set_attrs<64, sdpa::kFP16, true>(),
+                            set_attrs<128, sdpa::kBF16, true>(), set_attrs<128, sdpa::kFP16, true>()};
         for (cudaError_t x : es)
             if (x != cudaSuccess && st.err == cudaSuccess)
                 st.err = x;
@@ -243,7 +246,7 @@ bool valid_scale(float x)
 // bytes, or 64 when a row is 64 bytes), 1 head, 128 rows, 1 batch}, matching
 // swizzle, zero fill out of bounds (ragged sequence tails).
 bool encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int D, int H, int S, int B,
-                const Strides& st)
+                const Strides& st, int box_h, int box_s)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
@@ -253,7 +256,7 @@ bool encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int 
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)st.h * elem_bytes, (cuuint64_t)st.s * elem_bytes,
                                    (cuuint64_t)st.b * elem_bytes};
-    const cuuint32_t box[4] = {(cuuint32_t)(swz / elem_bytes), 1, (cuuint32_t)sdpa::kBlockM, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)(swz / elem_bytes), (cuuint32_t)box_h, (cuuint32_t)box_s, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
@@ -266,7 +269,7 @@ bool encode_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int 
 struct MapKey {
     const void* base;
     long long sb, ss, sh;
-    int dt, elem_bytes, D, H, S, B;
+    int dt, elem_bytes, D, H, S, B, box_h, box_s;
 };
 
 struct MapCache {
@@ -279,8 +282,10 @@ struct MapCache {
 
 thread_local MapCache t_maps;
 
+// box_h x box_s (heads x rows) per copy: 1 x 128, or G x 128 / G for packed
+// query tiles.
 bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int D, int H, int S, int B,
-              const Strides& st)
+              const Strides& st, int box_h = 1, int box_s = sdpa::kBlockM)
 {
     MapKey k;
     std::memset(&k, 0, sizeof k);                    // padding bytes take part in the comparison
@@ -294,13 +299,15 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
     k.H = H;
     k.S = S;
     k.B = B;
+    k.box_h = box_h;
+    k.box_s = box_s;
     MapCache& c = t_maps;
     for (int i = 0; i < MapCache::kSize; ++i)
         if (c.used[i] && std::memcmp(&c.key[i], &k, sizeof k) == 0) {
             *map = c.map[i];
             return true;
         }
-    if (!encode_map(map, base, dt, elem_bytes, D, H, S, B, st))
+    if (!encode_map(map, base, dt, elem_bytes, D, H, S, B, st, box_h, box_s))
         return false;
     const int slot = c.next;
     c.next = (c.next + 1) % MapCache::kSize;
@@ -310,15 +317,25 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
     return true;
 }
 
-template <int D, int KIND>
+template <int D, int KIND, bool kPacked = false>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const sdpa::Params& p,
                    int sm_count, cudaStream_t stream)
 {
     // persistent: one CTA per SM (each takes all 512 TMEM columns)
     const unsigned grid = static_cast<unsigned>(p.n_units < sm_count ? p.n_units : sm_count);
-    sdpa::sdpa_fwd_kernel<D, KIND><<<grid, sdpa::kThreads, sdpa::Layout<D, KIND>::kSmemBytes, stream>>>(tq, tk, tv,
-                                                                                                          p);
-    return cudaGetLastError();
+    sdpa::sdpa_fwd_kernel<D, KIND, kPacked>
+        <<<grid, sdpa::kThreads, sdpa::Layout<D, KIND>::kSmemBytes, stream>>>(tq, tk, tv, p);
+    cudaError_t e = cudaGetLastError();
+    if constexpr (kPacked) {
+        if (e == cudaSuccess && p.part_o) {
+            // merge the key-range splits: one warp per output row
+            const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
+            sdpa::sdpa_combine_kernel<D, KIND != sdpa::kFP16>
+                <<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(p);
+            e = cudaGetLastError();
+        }
+    }
+    return e;
 }
 
 sdpa::Params make_params(const Args& a, double score_scale, float out_scale, int causal)
@@ -408,6 +425,110 @@ sdpa_status_t run(const Args& a, float scale, const float* descales, int causal,
     return SDPA_OK;
 }
 
+// Packed (decode) pass plan: the G = Hq / Hkv query heads of a KV head are
+// stacked into Q tiles (G must divide 128), and with a workspace the key
+// range is split so that there are about two units per SM, each split at
+// least 4 key tiles long.
+struct DecodePlan {
+    int n_pairs, n_splits, tiles_per_split;
+    long long units;
+    size_t workspace_bytes;          // 0 when there is one split
+};
+
+DecodePlan plan_decode(const Shape& s, int sm_count, bool split)
+{
+    DecodePlan d{};
+    const int G = s.Hq / s.Hkv;
+    const long long rows_packed = static_cast<long long>(s.Sq) * G;
+    d.n_pairs = static_cast<int>((rows_packed + sdpa::kUnitRows - 1) / sdpa::kUnitRows);
+    const long long base = static_cast<long long>(s.B) * s.Hkv * d.n_pairs;
+    const int n_ktiles = (s.Skv + sdpa::kBlockN - 1) / sdpa::kBlockN;
+    int splits = 1;
+    if (split) {
+        const long long want = (2ll * sm_count + base - 1) / base;
+        const int max_splits = n_ktiles / 4 > 1 ? n_ktiles / 4 : 1;
+        splits = static_cast<int>(want < max_splits ? want : max_splits);
+        if (splits < 1)
+            splits = 1;
+    }
+    d.tiles_per_split = (n_ktiles + splits - 1) / splits;
+    d.n_splits = (n_ktiles + d.tiles_per_split - 1) / d.tiles_per_split;
+    d.units = base * d.n_splits;
+    const long long rows = static_cast<long long>(s.B) * s.Hq * s.Sq;
+    d.workspace_bytes = d.n_splits > 1 ? static_cast<size_t>(rows) * d.n_splits * (s.D + 1) * sizeof(float) : 0;
+    return d;
+}
+
+sdpa_status_t run_decode(const Args& a, float scale, sdpa_dtype_t dtype, void* ws, size_t ws_bytes, void* stream)
+{
+    if (dtype != SDPA_DTYPE_BF16 && dtype != SDPA_DTYPE_FP16)
+        return SDPA_ERR_DTYPE;
+    sdpa_status_t st = check_common(a, 2, 2);
+    if (st != SDPA_OK)
+        return st;
+    if (!valid_scale(scale))
+        return SDPA_ERR_SCALE;
+    const Shape& s = a.s;
+    const int G = s.Hq / s.Hkv;
+    if (sdpa::kBlockM % G != 0)
+        return SDPA_ERR_HEADS;
+    if (ws && !aligned16(ws))
+        return SDPA_ERR_WORKSPACE;
+
+    int dev = 0, sm_count = 0;
+    st = device_ready(&dev, &sm_count);
+    if (st != SDPA_OK)
+        return st;
+    const DecodePlan d = plan_decode(s, sm_count, ws != nullptr);
+    if (d.units > INT32_MAX)
+        return SDPA_ERR_BAD_SHAPE;
+    if (d.workspace_bytes > ws_bytes)
+        return SDPA_ERR_WORKSPACE;
+    if (d.workspace_bytes) {
+        const long long wb = static_cast<long long>(d.workspace_bytes);
+        const long long q_bytes = span_bytes(a.q, s.B, s.Sq, s.Hq, s.D, 2);
+        const long long k_bytes = span_bytes(a.k, s.B, s.Skv, s.Hkv, s.D, 2);
+        const long long v_bytes = span_bytes(a.v, s.B, s.Skv, s.Hkv, s.D, 2);
+        const long long o_bytes = span_bytes(a.o, s.B, s.Sq, s.Hq, s.D, 2);
+        if (overlaps(ws, wb, a.Q, q_bytes) || overlaps(ws, wb, a.K, k_bytes) || overlaps(ws, wb, a.V, v_bytes) ||
+            overlaps(ws, wb, a.O, o_bytes) ||
+            (a.lse && overlaps(ws, wb, a.lse, static_cast<long long>(s.B) * s.Hq * s.Sq * 4)))
+            return SDPA_ERR_ALIAS;
+    }
+
+    const CUtensorMapDataType dt =
+        dtype == SDPA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, a.Q, dt, 2, s.D, s.Hq, s.Sq, s.B, a.q, G, sdpa::kBlockM / G) ||
+        !make_map(&tk, a.K, dt, 2, s.D, s.Hkv, s.Skv, s.B, a.k) ||
+        !make_map(&tv, a.V, dt, 2, s.D, s.Hkv, s.Skv, s.B, a.v))
+        return cuda_fail(cudaErrorInvalidValue);
+
+    sdpa::Params p = make_params(a, scale, 1.f, 0);
+    p.n_pairs = d.n_pairs;
+    p.n_units = static_cast<int>(d.units);
+    p.tiles_per_split = d.tiles_per_split;
+    p.n_splits = d.n_splits;
+    if (d.workspace_bytes) {
+        const long long rows = static_cast<long long>(s.B) * s.Hq * s.Sq;
+        p.part_o = static_cast<float*>(ws);
+        p.part_lse = p.part_o + rows * d.n_splits * s.D;
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (dtype == SDPA_DTYPE_BF16)
+        e = s.D == 32 ? launch<32, sdpa::kBF16, true>(tq, tk, tv, p, sm_count, cs)
+          : s.D == 64 ? launch<64, sdpa::kBF16, true>(tq, tk, tv, p, sm_count, cs)
+                      : launch<128, sdpa::kBF16, true>(tq, tk, tv, p, sm_count, cs);
+    else
+        e = s.D == 32 ? launch<32, sdpa::kFP16, true>(tq, tk, tv, p, sm_count, cs)
+          : s.D == 64 ? launch<64, sdpa::kFP16, true>(tq, tk, tv, p, sm_count, cs)
+                      : launch<128, sdpa::kFP16, true>(tq, tk, tv, p, sm_count, cs);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    return SDPA_OK;
+}
+
 Args make_args(const void* Q, const void* K, const void* V, void* O, float* lse, int B, int Hq, int Hkv, int Sq,
                int Skv, int D, const sdpa_layout_t* ql, const sdpa_layout_t* kl, const sdpa_layout_t* vl,
                const sdpa_layout_t* ol)
@@ -457,6 +578,26 @@ sdpa_status_t sdpa_fwd_fp8_ex(const void* Q, const void* K, const void* V, void*
     return run(a, scale, descales, causal, SDPA_DTYPE_E4M3, stream);
 }
 
+sdpa_status_t sdpa_fwd_decode(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
+                              int Hkv, int Sq, int Skv, int D, const sdpa_layout_t* q_layout,
+                              const sdpa_layout_t* k_layout, const sdpa_layout_t* v_layout,
+                              const sdpa_layout_t* o_layout, float scale, sdpa_dtype_t dtype, void* workspace,
+                              size_t workspace_bytes, void* stream)
+{
+    const Args a = make_args(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, q_layout, k_layout, v_layout, o_layout);
+    return run_decode(a, scale, dtype, workspace, workspace_bytes, stream);
+}
+
+size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int D)
+{
+    if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Skv < 1 || Hq % Hkv != 0 || (D != 32 && D != 64 && D != 128))
+        return 0;
+    int dev = 0, sm_count = 0;
+    if (device_ready(&dev, &sm_count) != SDPA_OK)
+        return 0;
+    return plan_decode(Shape{B, Hq, Hkv, Sq, Skv, D}, sm_count, true).workspace_bytes;
+}
+
 const char* sdpa_status_string(sdpa_status_t status)
 {
     switch (status) {
@@ -472,6 +613,7 @@ const char* sdpa_status_string(sdpa_status_t status)
     case SDPA_ERR_ALIAS: return "output overlaps an input";
     case SDPA_ERR_CUDA: return "CUDA error";
     case SDPA_ERR_LAYOUT: return "unusable strides";
+    case SDPA_ERR_WORKSPACE: return "workspace too small or not 16-byte aligned";
     }
     return "unknown status";
 }
@@ -502,7 +644,7 @@ sdpa_status_t sdpa_device_error(unsigned int* code)
 
 int sdpa_abi_version(void)
 {
-    return 2;
+    return 3;
 }
 
 }  // extern "C"

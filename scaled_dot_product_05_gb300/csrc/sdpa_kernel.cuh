@@ -89,6 +89,13 @@ struct Params {
     int causal;
     float scale_log2;                // scale * log2(e) (* descale_q * descale_k for E4M3)
     float out_scale;                 // descale_v for E4M3, else 1
+    // packed (decode) mode only: key tiles per split, splits, and the split
+    // results (null with one split): per packed row (b, h, s) and split, O / l
+    // in fp32 [B][Hq][Sq][n_splits][D] and the LSE [B][Hq][Sq][n_splits]
+    int tiles_per_split;
+    int n_splits;
+    float* part_o;
+    float* part_lse;
 };
 
 // Element kinds of Q, K and V.
@@ -213,12 +220,38 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
 // last query rows see the most keys).
 struct Unit {
     int b, hq, hkv, pair;
-    int n_kv[2];                     // key tiles visited by Q tile 0 / 1
+    int n;                           // key tiles loaded for the unit: kv0 .. kv0 + n - 1
+    int kv0;
+    int split;                       // packed mode: which key range
+    int n_kv[2];                     // key tiles visited by Q tile 0 / 1 (the first n_kv[t]; 0 = tile unused)
 };
 
+// Packed (decode) mode: the Hq / Hkv = G query heads that read one KV head are
+// stacked into the M rows of a Q tile, row r = s * G + h (query position s,
+// head h of the group), so a K/V tile serves every head of the group at once;
+// the key range may be split over several units.  Non-causal only.
+// Unit u -> (KV head, batch, packed-row pair, split), KV head fastest.
+template <bool kPacked>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u)
 {
     Unit w;
+    if constexpr (kPacked) {
+        w.hkv = u % p.Hkv;
+        int rest = u / p.Hkv;
+        w.b = rest % p.B;
+        rest /= p.B;
+        w.pair = rest % p.n_pairs;
+        w.split = rest / p.n_pairs;
+        w.hq = w.hkv * p.group;
+        w.kv0 = w.split * p.tiles_per_split;
+        w.n = min(p.n_ktiles - w.kv0, p.tiles_per_split);
+        const int rows = p.Sq * p.group;                   // packed rows of one (b, KV head)
+        w.n_kv[0] = w.n;                                    // the pair exists, so tile 0 has rows
+        w.n_kv[1] = (w.pair * kUnitRows + kBlockM < rows) ? w.n : 0;
+        return w;
+    }
+    w.split = 0;
+    w.kv0 = 0;
     const int bh_count = p.B * p.Hq;
     w.pair = u / bh_count;
     if (p.causal)
@@ -233,6 +266,7 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u)
     } else {
         w.n_kv[0] = w.n_kv[1] = p.n_ktiles;
     }
+    w.n = w.n_kv[1];                 // tile 1 visits at least as many key tiles as tile 0
     return w;
 }
 
@@ -281,7 +315,7 @@ __device__ __forceinline__ uint64_t desc_join(uint32_t hi, uint32_t lo)
 // kKeysPerStep keys is kKeysPerStep rows of kSwz bytes, the next chunk of D
 // columns kChunkBytes further (LBO).  The E4M3 P tile and the ones tile have
 // 128-byte rows: one 128-byte swizzle span, 8-row groups 1024 bytes apart.
-template <int D, int KIND, int NK, int NV>
+template <int D, int KIND, bool kPacked, int NK, int NV>
 __device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
                                             uint32_t tmem, uint32_t sQ, uint32_t sK)
 {
@@ -294,7 +328,7 @@ __device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* b
     uint32_t ck = 0;                     // K ring position
     uint32_t ns[2] = {0, 0};             // S tiles issued per Q tile
     int prev = -1;                       // Q tile of the last S issued
-    uint32_t units = 0;
+    uint32_t ua[2] = {0, 0};             // units in which Q tile 0 / 1 took part
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int u = unit_of_round(p, r);
@@ -302,15 +336,15 @@ __device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* b
             break;
         if (u < 0)
             continue;
-        const Unit w = decode_unit(p, u);
-        const int n = w.n_kv[1];         // tile 1 visits at least as many key tiles as tile 0
+        const Unit w = decode_unit<kPacked>(p, u);
+        const int n = w.n;
         for (int j = 0; ok && j < n; ++j) {
             ok = wait_bar(smem_u32(&bars->k_full[ck % NK]), (ck / NK) & 1, abort, kErrWaitMma + 3);
             for (int t = 0; ok && t < 2; ++t) {
                 if (j >= w.n_kv[t])
                     continue;
                 if (j == 0)
-                    ok = wait_bar(smem_u32(&bars->q_full[t]), units & 1, abort, kErrWaitMma + 1 + t);
+                    ok = wait_bar(smem_u32(&bars->q_full[t]), ua[t] & 1, abort, kErrWaitMma + 1 + t);
                 // the previous S in this region has been read out of it: the
                 // last S of either tile (shared region) or of this tile
                 const int pt = L::kSharedS ? prev : (ns[t] > 0 ? t : -1);
@@ -343,7 +377,8 @@ __device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* b
             mma_commit(smem_u32(&bars->k_empty[ck % NK]));
             ++ck;
         }
-        ++units;
+        for (int t = 0; t < 2; ++t)
+            ua[t] += (w.n_kv[t] > 0) ? 1u : 0u;
     }
     // every MMA this thread issued completes before TMEM is released
     mma_commit(smem_u32(&bars->drain[2]));
@@ -355,7 +390,7 @@ __device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* b
 // (K-major, keys contiguous) comes from shared memory, and l_t (+)= P_t x
 // ones.  Both P V threads release every V slot of the unit (barrier count 2),
 // tile 0 also the causal key tile it does not visit.
-template <int D, int KIND, int NK, int NV>
+template <int D, int KIND, bool kPacked, int NK, int NV>
 __device__ __forceinline__ void mma_issue_pv(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
                                              uint32_t tmem, uint32_t sV, uint32_t sP, uint32_t sOnes, int t)
 {
@@ -375,7 +410,7 @@ __device__ __forceinline__ void mma_issue_pv(const Params& p, Barriers<NK, NV>* 
     const uint32_t ones_lo = (sOnes >> 4) | (1u << 16);
     uint32_t cv = 0;                     // V ring position
     uint32_t npv = 0;                    // P V groups issued
-    uint32_t units = 0;
+    uint32_t units = 0;                  // units in which this Q tile took part
     bool ok = true;
     for (int r = 0; ok; ++r) {
         const int u = unit_of_round(p, r);
@@ -383,14 +418,14 @@ __device__ __forceinline__ void mma_issue_pv(const Params& p, Barriers<NK, NV>* 
             break;
         if (u < 0)
             continue;
-        const Unit w = decode_unit(p, u);
-        const int n = w.n_kv[1];
+        const Unit w = decode_unit<kPacked>(p, u);
+        const int n = w.n;
         const int nt = w.n_kv[t];
         for (int j = 0; ok && j < n; ++j, ++cv) {
             ok = wait_bar(smem_u32(&bars->v_full[cv % NV]), (cv / NV) & 1, abort, kErrWaitMma + 5);
             if (!ok)
                 break;
-            if (j >= nt) {               // tile 0 past its last causal key tile: release V_j
+            if (j >= nt) {               // past this tile's last key tile (or tile unused): release V_j
                 mbar_arrive(smem_u32(&bars->v_empty[cv % NV]));
                 continue;
             }
@@ -423,13 +458,13 @@ __device__ __forceinline__ void mma_issue_pv(const Params& p, Barriers<NK, NV>* 
                 mma_commit(smem_u32(&bars->o_full[t]));
             ++npv;
         }
-        ++units;
+        units += (nt > 0) ? 1u : 0u;
     }
     mma_commit(smem_u32(&bars->drain[t]));
     drain_wait(smem_u32(&bars->drain[t]), 0);
 }
 
-template <int D, int KIND>
+template <int D, int KIND, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
 sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const Params p)
@@ -509,9 +544,14 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (nq[t] > 0 && !wait_bar(smem_u32(&bars->q_empty[t]), (nq[t] - 1) & 1, abort, kErrWaitLoad + 1 + t))
                     return false;
                 mbar_arrive_expect_tx(smem_u32(&bars->q_full[t]), L::kTileBytes);
+                // packed: the tensor map's box is {chunk, G heads, 128 / G positions},
+                // so one copy brings rows s * G + h of the KV head's query heads
+                const int r0 = w.pair * kUnitRows + t * kBlockM;
+                const int h = kPacked ? w.hkv * p.group : w.hq;
+                const int s0 = kPacked ? r0 / p.group : r0;
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_4d(sQ + t * L::kTileBytes + c * L::kChunkBytes, &tm_q, smem_u32(&bars->q_full[t]),
-                                c * (L::kSwz / L::kEsize), w.hq, w.pair * kUnitRows + t * kBlockM, w.b);
+                                c * (L::kSwz / L::kEsize), h, s0, w.b);
                 ++nq[t];
                 return true;
             };
@@ -522,7 +562,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive_expect_tx(smem_u32(&bars->k_full[s]), L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_4d(sK + s * L::kTileBytes + c * L::kChunkBytes, &tm_k, smem_u32(&bars->k_full[s]),
-                                c * (L::kSwz / L::kEsize), w.hkv, j * kBlockN, w.b);
+                                c * (L::kSwz / L::kEsize), w.hkv, (w.kv0 + j) * kBlockN, w.b);
                 ++nk;
                 return true;
             };
@@ -533,7 +573,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive_expect_tx(smem_u32(&bars->v_full[s]), L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_4d(sV + s * L::kTileBytes + c * L::kChunkBytes, &tm_v, smem_u32(&bars->v_full[s]),
-                                c * (L::kSwz / L::kEsize), w.hkv, j * kBlockN, w.b);
+                                c * (L::kSwz / L::kEsize), w.hkv, (w.kv0 + j) * kBlockN, w.b);
                 ++nv;
                 return true;
             };
@@ -543,9 +583,9 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     break;
                 if (u < 0)
                     continue;
-                const Unit w = decode_unit(p, u);
-                const int n = w.n_kv[1];
-                ok = load_q(w, 0) && load_k(w, 0) && load_q(w, 1) && load_v(w, 0);
+                const Unit w = decode_unit<kPacked>(p, u);
+                const int n = w.n;
+                ok = load_q(w, 0) && load_k(w, 0) && (w.n_kv[1] == 0 || load_q(w, 1)) && load_v(w, 0);
                 for (int j = 1; ok && j < n; ++j)
                     ok = load_k(w, j) && load_v(w, j);
             }
@@ -563,11 +603,12 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       } else if (warp == kSMmaWarp) {
         // ============================= S issuer =============================
         if (lane == 0)
-            mma_issue_s<D, KIND, NK, NV>(p, bars, abort, tmem, sQ, sK);
+            mma_issue_s<D, KIND, kPacked, NK, NV>(p, bars, abort, tmem, sQ, sK);
       } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
         // =========================== P V issuers ============================
         if (lane == 0) {
-            mma_issue_pv<D, KIND, NK, NV>(p, bars, abort, tmem, sV, sP, smem_u32(smem + L::kOffOnes), warp - kMmaWarp);
+            mma_issue_pv<D, KIND, kPacked, NK, NV>(p, bars, abort, tmem, sV, sP, smem_u32(smem + L::kOffOnes),
+                                                  warp - kMmaWarp);
         }
       }
     } else {
@@ -605,9 +646,15 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 break;
             if (u < 0)
                 continue;
-            const Unit w = decode_unit(p, u);
+            const Unit w = decode_unit<kPacked>(p, u);
             const int n = w.n_kv[t];
-            const int q_idx = w.pair * kUnitRows + t * kBlockM + row;
+            if (n == 0)
+                continue;                                  // this Q tile has no rows in the unit
+            // this thread's row: query position q_idx of head hq (packed:
+            // row r of the KV head's stacked heads, r = q_idx * G + head)
+            const int r_all = w.pair * kUnitRows + t * kBlockM + row;
+            const int q_idx = kPacked ? r_all / p.group : r_all;
+            const int hq = kPacked ? w.hkv * p.group + r_all % p.group : w.hq;
             int limit = p.Skv - 1;                         // last key this row sees
             if (p.causal && q_idx < limit)
                 limit = q_idx;
@@ -625,7 +672,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // the S region is free for the next S as soon as it is read
                 tc_fence_before_sync();
                 mbar_arrive(smem_u32(&bars->s_free[t]));
-                const int k0 = j * kBlockN;
+                const int k0 = (w.kv0 + j) * kBlockN;
                 if (k0 + kBlockN - 1 > limit) {
 #pragma unroll
                     for (int i = 0; i < 128; ++i)
@@ -754,22 +801,33 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_arrive(smem_u32(&bars->o_empty[t]));
             if (q_idx < p.Sq) {
                 const float inv_l = p.out_scale / l;
-                if (p.lse) {
-                    // log sum_j exp(s_j) = ln 2 * (m + log2 l): m is the max of
-                    // s * log2(e) the weights were taken against, l their sum
-                    // (E4M3: of the weights times 56)
-                    const float lg = kFP8 ? log2f(l) - kLog2P8Scale : log2f(l);
-                    p.lse[((int64_t)w.b * p.Hq + w.hq) * p.Sq + q_idx] = (m + lg) * kLn2;
-                }
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.O) +
-                                                      ((int64_t)w.b * p.o_sb + (int64_t)q_idx * p.o_ss +
-                                                       (int64_t)w.hq * p.o_sh) * 2);
+                // log sum_j exp(s_j) = ln 2 * (m + log2 l): m is the max of
+                // s * log2(e) the weights were taken against, l their sum
+                // (E4M3: of the weights times 56)
+                const float lse = (m + (kFP8 ? log2f(l) - kLog2P8Scale : log2f(l))) * kLn2;
+                const int64_t row_id = ((int64_t)w.b * p.Hq + hq) * p.Sq + q_idx;
+                if (kPacked && p.part_o) {
+                    // one split of the key range: O / l in fp32 and the LSE, merged later
+                    const int64_t slot = row_id * p.n_splits + w.split;
+                    p.part_lse[slot] = lse;
+                    float4* dst = reinterpret_cast<float4*>(p.part_o + slot * D);
 #pragma unroll
-                for (int v = 0; v < D / 8; ++v)
-                    dst[v] = make_uint4(pack2<kOutBF16>(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
-                                        pack2<kOutBF16>(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l),
-                                        pack2<kOutBF16>(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l),
-                                        pack2<kOutBF16>(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l));
+                    for (int v = 0; v < D / 4; ++v)
+                        dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                             __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+                } else {
+                    if (p.lse)
+                        p.lse[row_id] = lse;
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.O) +
+                                                          ((int64_t)w.b * p.o_sb + (int64_t)q_idx * p.o_ss +
+                                                           (int64_t)hq * p.o_sh) * 2);
+#pragma unroll
+                    for (int v = 0; v < D / 8; ++v)
+                        dst[v] = make_uint4(pack2<kOutBF16>(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
+                                            pack2<kOutBF16>(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l),
+                                            pack2<kOutBF16>(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l),
+                                            pack2<kOutBF16>(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l));
+                }
             }
             ++units;
         }
@@ -782,6 +840,58 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_after_sync();
         tmem_dealloc(tmem, L::kTmemCols);
     }
+}
+
+// Merges the key-range splits of a packed (decode) pass.  Split k of a row
+// holds its normalised output O_k = sum_{j in k} w_j V_j / l_k and lse_k =
+// log l_k (with the max folded in); over all splits
+//     LSE = log sum_k exp(lse_k),   O = sum_k exp(lse_k - LSE) O_k,
+// the same softmax over the whole key range.  One warp per row (b, hq, s);
+// each lane merges D / 32 consecutive columns.
+template <int D, bool kOutBF16>
+__global__ void __launch_bounds__(128) sdpa_combine_kernel(const Params p)
+{
+    constexpr int kCols = D / 32;
+    const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= (int64_t)p.B * p.Hq * p.Sq)
+        return;
+    const int S = p.n_splits;
+    const float* lse = p.part_lse + row * S;
+    float mx = -INFINITY;
+    for (int k = 0; k < S; ++k)
+        mx = fmaxf(mx, lse[k]);
+    float den = 0.f;
+    float acc[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; ++c)
+        acc[c] = 0.f;
+    for (int k = 0; k < S; ++k) {
+        const float w = expf(lse[k] - mx);
+        den += w;
+        const float* o = p.part_o + (row * S + k) * D + lane * kCols;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+            acc[c] += w * o[c];
+    }
+    const float inv = 1.f / den;
+    const int q = (int)(row % p.Sq);
+    const int64_t bh = row / p.Sq;
+    const int hq = (int)(bh % p.Hq);
+    const int b = (int)(bh / p.Hq);
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.O) + (int64_t)b * p.o_sb + (int64_t)q * p.o_ss +
+                    (int64_t)hq * p.o_sh + lane * kCols;
+    if constexpr (kCols % 2 == 0) {
+#pragma unroll
+        for (int c = 0; c < kCols; c += 2)
+            *reinterpret_cast<uint32_t*>(dst + c) = pack2<kOutBF16>(acc[c] * inv, acc[c + 1] * inv);
+    } else {
+#pragma unroll
+        for (int c = 0; c < kCols; ++c)
+            dst[c] = (uint16_t)(pack2<kOutBF16>(acc[c] * inv, 0.f) & 0xffffu);
+    }
+    if (p.lse && lane == 0)
+        p.lse[row] = mx + logf(den);
 }
 
 }  // namespace sdpa

@@ -41,7 +41,7 @@ def test_exports_every_declared_function(lib):
 
 def test_abi_version_and_strings(lib):
     assert lib.sdpa_abi_version() >= 1
-    for code in range(12):
+    for code in range(13):
         s = lib.sdpa_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.sdpa_status_string(99).decode() == "unknown status"
@@ -147,3 +147,26 @@ def test_fp8_ex_checks(lib):
              s(0.125), s(1), s(1), s(1), 0, None) == 11
     assert f(QP, KP, VP, OP, None, 1, 2, 2, 128, 128, 64, None, None, None, None,
              s(0.125), s(1), s(-1), s(1), 0, None) == 7
+
+
+def call_decode(lib, ws=None, ws_bytes=0, **kw):
+    a = dict(GOOD, **kw)
+    return lib.sdpa_fwd_decode(QP, KP, VP, OP, None, a["B"], a["Hq"], a["Hkv"], 1, a["Skv"], a["D"],
+                               None, None, None, None, ctypes.c_float(a["scale"]), a["dtype"], ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=12, Hkv=4), 4),          # G = 3 does not divide the 128 rows of a tile
+    (dict(Hq=8, Hkv=3), 4),           # not a multiple
+    (dict(dtype=2), 6),               # E4M3 has no decode pass
+    (dict(ws=0x50000008, ws_bytes=1 << 20), 12),   # workspace not 16-byte aligned
+    (dict(D=48), 5),
+])
+def test_decode_rejects_before_any_cuda_call(lib, kw, status):
+    assert call_decode(lib, **kw) == status
+
+
+def test_decode_workspace_query_rejects_bad_sizes(lib):
+    assert lib.sdpa_decode_workspace_bytes(0, 8, 2, 1, 1000, 128) == 0
+    assert lib.sdpa_decode_workspace_bytes(1, 8, 3, 1, 1000, 128) == 0
+    assert lib.sdpa_decode_workspace_bytes(1, 8, 2, 1, 1000, 96) == 0
