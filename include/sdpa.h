@@ -179,6 +179,26 @@ sdpa_status_t sdpa_fwd_decode(const void *Q, const void *K, const void *V, void 
                               void *stream);
 
 /*
+ * sdpa_fwd_decode without a caller workspace and without allocating: the
+ * split results go to a 32 MiB scratch array that the library holds in
+ * device memory (one per device, part of the loaded module).  The codelab
+ * has no counterpart to this entry point; it exists for callers that cannot
+ * allocate or pass a workspace.
+ *   - Plans that would need more than the scratch return SDPA_ERR_WORKSPACE
+ *     (none do on a device with <= 240 SMs at D <= 128).
+ *   - Nothing in the scratch has to start at zero: each call writes every
+ *     slot its merge step reads.
+ *   - Race: all calls on a device share the one scratch array; calls must
+ *     not run at the same time (issue them on one stream, or order them).
+ * Arguments as for sdpa_fwd_decode.
+ */
+sdpa_status_t sdpa_fwd_decode_noalloc(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                      int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                                      const sdpa_layout_t *q_layout, const sdpa_layout_t *k_layout,
+                                      const sdpa_layout_t *v_layout, const sdpa_layout_t *o_layout,
+                                      float scale, sdpa_dtype_t dtype, void *stream);
+
+/*
  * Workspace bytes sdpa_fwd_decode needs for this shape on the current device
  * (0: no split, or invalid sizes).  Initialises the library on the current
  * device on first use.

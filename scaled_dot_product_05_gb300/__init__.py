@@ -14,7 +14,7 @@ import torch
 from . import _abi
 from ._abi import SdpaError, check, lib, status_string
 
-__all__ = ["sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_fwd_decode",
+__all__ = ["sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_fwd_decode", "sdpa_fwd_decode_noalloc",
            "decode_workspace_bytes", "sdpa_status_string", "sdpa_device_error", "SdpaError", "lib"]
 
 _DTYPE = {torch.bfloat16: _abi.SDPA_DTYPE_BF16, torch.float16: _abi.SDPA_DTYPE_FP16}
@@ -183,6 +183,29 @@ def sdpa_fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.
                                 B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq), ctypes.byref(lk), ctypes.byref(lv),
                                 ctypes.byref(lo), float(scale), _DTYPE.get(q.dtype, 99), ws, ws_bytes,
                                 _stream_ptr(stream, q.device.index)))
+    return o
+
+
+def sdpa_fwd_decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                            lse: torch.Tensor | None = None, *, scale: float | None = None,
+                            stream=None) -> torch.Tensor:
+    """:func:`sdpa_fwd_decode` with the library's own device scratch instead
+    of a workspace (allocates nothing; calls must not run concurrently)."""
+    for t in (q, k, v, o):
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+    if q.dtype != k.dtype or q.dtype != v.dtype or o.dtype != q.dtype or tuple(o.shape) != tuple(q.shape):
+        raise ValueError("q, k, v, o must share a dtype; o is shaped like q")
+    B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+    if tuple(k.shape) != tuple(v.shape):
+        raise ValueError("K and V must have the same shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lq, lk, lv, lo = _layout(q), _layout(k), _layout(v), _layout(o)
+    check(lib().sdpa_fwd_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                        _lse_ptr(lse, B, Hq, Sq), B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq),
+                                        ctypes.byref(lk), ctypes.byref(lv), ctypes.byref(lo), float(scale),
+                                        _DTYPE.get(q.dtype, 99), _stream_ptr(stream, q.device.index)))
     return o
 
 

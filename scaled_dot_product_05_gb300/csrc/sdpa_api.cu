@@ -19,6 +19,16 @@ namespace {
 
 thread_local int t_last_cuda_error = 0;
 
+// Scratch of sdpa_fwd_decode_noalloc: a file-scope device array (one instance
+// per device, allocated with the module, never by a call).  A split plan
+// needs at most rows * splits * (D + 1) * 4 bytes with B * Hkv * pairs *
+// splits <= #SMs, i.e. #SMs * 256 * 129 * 4 bytes (about 20 MB on 152 SMs);
+// larger plans are rejected.  Nothing in it needs to start at zero: every
+// slot the merge reads is written earlier in the same call.  Calls that use
+// it must not overlap in time (same stream, or otherwise ordered).
+constexpr size_t kDecodeScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) float g_decode_scratch[kDecodeScratchBytes / sizeof(float)];
+
 sdpa_status_t cuda_fail(cudaError_t e)
 {
     t_last_cuda_error = static_cast<int>(e);
@@ -588,6 +598,30 @@ sdpa_status_t sdpa_fwd_decode(const void* Q, const void* K, const void* V, void*
 {
     const Args a = make_args(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, q_layout, k_layout, v_layout, o_layout);
     return run_decode(a, scale, dtype, workspace, workspace_bytes, stream);
+}
+
+sdpa_status_t sdpa_fwd_decode_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                                      int Hq, int Hkv, int Sq, int Skv, int D, const sdpa_layout_t* q_layout,
+                                      const sdpa_layout_t* k_layout, const sdpa_layout_t* v_layout,
+                                      const sdpa_layout_t* o_layout, float scale, sdpa_dtype_t dtype, void* stream)
+{
+    const Args a = make_args(Q, K, V, O, LSE, B, Hq, Hkv, Sq, Skv, D, q_layout, k_layout, v_layout, o_layout);
+    // argument checks first, as for every entry point (run_decode repeats them)
+    if (dtype != SDPA_DTYPE_BF16 && dtype != SDPA_DTYPE_FP16)
+        return SDPA_ERR_DTYPE;
+    const sdpa_status_t st = check_common(a, 2, 2);
+    if (st != SDPA_OK)
+        return st;
+    if (!valid_scale(scale))
+        return SDPA_ERR_SCALE;
+    if (sdpa::kBlockM % (Hq / Hkv) != 0)
+        return SDPA_ERR_HEADS;
+    // the current device's instance of the library's scratch array
+    void* scratch = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&scratch, g_decode_scratch);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    return run_decode(a, scale, dtype, scratch, kDecodeScratchBytes, stream);
 }
 
 size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int D)

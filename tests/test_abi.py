@@ -170,3 +170,11 @@ def test_decode_workspace_query_rejects_bad_sizes(lib):
     assert lib.sdpa_decode_workspace_bytes(0, 8, 2, 1, 1000, 128) == 0
     assert lib.sdpa_decode_workspace_bytes(1, 8, 3, 1, 1000, 128) == 0
     assert lib.sdpa_decode_workspace_bytes(1, 8, 2, 1, 1000, 96) == 0
+
+
+def test_decode_noalloc_rejects_before_any_cuda_call(lib):
+    s = ctypes.c_float
+    f = lib.sdpa_fwd_decode_noalloc
+    assert f(QP, KP, VP, OP, None, 1, 12, 4, 1, 1000, 128, None, None, None, None, s(0.1), 0, None) == 4
+    assert f(None, KP, VP, OP, None, 1, 8, 2, 1, 1000, 128, None, None, None, None, s(0.1), 0, None) == 1
+    assert f(QP, KP, VP, OP, None, 1, 8, 2, 1, 1000, 128, None, None, None, None, s(0.1), 2, None) == 6
