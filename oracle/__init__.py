@@ -58,6 +58,8 @@ def _bind(lib):
     lib.oracle_sdpa_fwd.restype = ci
     lib.oracle_sdpa_fwd.argtypes = [cvp, cvp, cvp, ci, cd, cd, cd, cl, cl, cl, cl, cl, cl,
                                     cd, ci, cvp, cvp, ci]
+    lib.oracle_sdpa_bwd.restype = ci
+    lib.oracle_sdpa_bwd.argtypes = [cvp, cvp, cvp, cvp, ci, cl, cl, cl, cl, cl, cl, cd, ci, cvp, cvp, cvp, ci]
     lib.oracle_decode.restype = cd
     lib.oracle_decode.argtypes = [cvp, cl, ci, cd]
     lib.oracle_max_threads.restype = ci
@@ -167,6 +169,31 @@ def sdpa_reference(q, k, v, *, causal: bool, scale: float | None = None, dtype: 
 
 
 _last_threads = 0
+
+
+def sdpa_backward_reference(q, k, v, do, *, causal: bool, scale: float | None = None, dtype: str = "bf16",
+                            threads: int = 0, lib=None):
+    """fp64 gradients (dQ, dK, dV) of sum(dO * O) for O = attention(Q, K, V):
+    dQ [B, Sq, Hq, D], dK and dV [B, Skv, Hkv, D] (float64).  ``do`` has Q's
+    shape and element type ("bf16", "fp16", "f32" or "f64")."""
+    global _last_threads
+    lib = lib or load_library()
+    qa, ka, va, da = _raw(q, dtype), _raw(k, dtype), _raw(v, dtype), _raw(do, dtype)
+    B, Hq, Hkv, Sq, Skv, D = _check_shapes(qa, ka, va)
+    if da.shape != qa.shape:
+        raise ValueError("dO must be shaped like Q")
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    dq = np.empty((B, Sq, Hq, D), dtype=np.float64)
+    dk = np.empty((B, Skv, Hkv, D), dtype=np.float64)
+    dv = np.empty((B, Skv, Hkv, D), dtype=np.float64)
+    nt = lib.oracle_sdpa_bwd(qa.ctypes.data, ka.ctypes.data, va.ctypes.data, da.ctypes.data, DTYPES[dtype],
+                             B, Hq, Hkv, Sq, Skv, D, float(scale), int(bool(causal)),
+                             dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, int(threads))
+    if nt < 0:
+        raise ValueError("oracle rejected the arguments")
+    _last_threads = nt
+    return dq, dk, dv
 
 
 def last_threads() -> int:

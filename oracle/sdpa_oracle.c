@@ -290,6 +290,101 @@ int oracle_sdpa_fwd(const void *Q, const void *K, const void *V, int dtype,
     return failed ? -1 : nt;
 }
 
+/*
+ * Backward pass of the same attention, for an upstream gradient dO (shaped
+ * like O, same element type as Q): with the scores s_ij = scale q_i . k_j,
+ * the softmax P_i. over the visible keys, O_i = sum_j P_ij v_j and the loss
+ * sum_i dO_i . O_i, the chain rule through section 1's three steps gives
+ *     dV_j  = sum_i P_ij dO_i
+ *     dP_ij = dO_i . v_j
+ *     dS_ij = P_ij (dP_ij - sum_l P_il dP_il)       (softmax Jacobian)
+ *     dQ_i  = scale sum_j dS_ij k_j
+ *     dK_j  = scale sum_i dS_ij q_i
+ * Masked keys have P_ij = 0.  With grouped heads each KV head sums the
+ * contributions of its G query heads.  dQ is [B][Sq][Hq][D], dK and dV are
+ * [B][Skv][Hkv][D], all doubles.  Parallel over (b, KV head), so no two
+ * threads add into the same dK / dV row.  Returns the number of threads
+ * used, or -1 on an invalid argument.
+ */
+int oracle_sdpa_bwd(const void *Q, const void *K, const void *V, const void *dO, int dtype,
+                    long B, long Hq, long Hkv, long Sq, long Skv, long D,
+                    double scale, int causal, double *dQ, double *dK, double *dV, int nthreads)
+{
+    problem_t p = {Q, K, V, dtype, 1.0, 1.0, 1.0, B, Hq, Hkv, Sq, Skv, D, scale, causal};
+    if (!valid_problem(&p) || !dO || !dQ || !dK || !dV || dtype == ORACLE_E4M3)
+        return -1;
+    const long G = Hq / Hkv;
+    int nt = resolve_threads(nthreads);
+    int failed = 0;
+    memset(dK, 0, sizeof(double) * (size_t)(B * Skv * Hkv * D));
+    memset(dV, 0, sizeof(double) * (size_t)(B * Skv * Hkv * D));
+#pragma omp parallel num_threads(nt)
+    {
+        double *P = (double *)malloc(sizeof(double) * (size_t)Skv);
+        double *dP = (double *)malloc(sizeof(double) * (size_t)Skv);
+        if (!P || !dP) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long bg = 0; bg < B * Hkv; ++bg) {
+            if (!P || !dP)
+                continue;
+            const long b = bg / Hkv, g = bg % Hkv;
+            for (long hq = g * G; hq < (g + 1) * G; ++hq) {
+                for (long i = 0; i < Sq; ++i) {
+                    /* keys 0..i under the causal mask (lower triangle) */
+                    const long n_vis = (causal && i + 1 < Skv) ? i + 1 : Skv;
+                    /* forward: softmax of the visible scores */
+                    double m = -INFINITY;
+                    for (long j = 0; j < n_vis; ++j) {
+                        double acc = 0.0;
+                        for (long d = 0; d < D; ++d)
+                            acc += load_elem(Q, bshd(b, i, hq, d, Sq, Hq, D), dtype, 1.0) *
+                                   load_elem(K, bshd(b, j, g, d, Skv, Hkv, D), dtype, 1.0);
+                        P[j] = acc * scale;
+                        if (P[j] > m)
+                            m = P[j];
+                    }
+                    double denom = 0.0;
+                    for (long j = 0; j < n_vis; ++j) {
+                        P[j] = exp(P[j] - m);
+                        denom += P[j];
+                    }
+                    for (long j = 0; j < n_vis; ++j)
+                        P[j] /= denom;
+                    /* dP_ij = dO_i . v_j and its P-weighted mean */
+                    double mean = 0.0;
+                    for (long j = 0; j < n_vis; ++j) {
+                        double acc = 0.0;
+                        for (long d = 0; d < D; ++d)
+                            acc += load_elem(dO, bshd(b, i, hq, d, Sq, Hq, D), dtype, 1.0) *
+                                   load_elem(V, bshd(b, j, g, d, Skv, Hkv, D), dtype, 1.0);
+                        dP[j] = acc;
+                        mean += P[j] * acc;
+                    }
+                    double *dq = dQ + bshd(b, i, hq, 0, Sq, Hq, D);
+                    for (long d = 0; d < D; ++d)
+                        dq[d] = 0.0;
+                    for (long j = 0; j < n_vis; ++j) {
+                        const double dS = P[j] * (dP[j] - mean);
+                        double *dk = dK + bshd(b, j, g, 0, Skv, Hkv, D);
+                        double *dv = dV + bshd(b, j, g, 0, Skv, Hkv, D);
+                        for (long d = 0; d < D; ++d) {
+                            dq[d] += scale * dS * load_elem(K, bshd(b, j, g, d, Skv, Hkv, D), dtype, 1.0);
+                            dk[d] += scale * dS * load_elem(Q, bshd(b, i, hq, d, Sq, Hq, D), dtype, 1.0);
+                            dv[d] += P[j] * load_elem(dO, bshd(b, i, hq, d, Sq, Hq, D), dtype, 1.0);
+                        }
+                    }
+                }
+            }
+        }
+        free(P);
+        free(dP);
+    }
+    return failed ? -1 : nt;
+}
+
 int oracle_max_threads(void)
 {
     return resolve_threads(0);

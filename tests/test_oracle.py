@@ -239,11 +239,75 @@ def pin_e4m3_descales(lib):
     np.testing.assert_allclose(o_v2, 2 * o8, rtol=0, atol=1e-13)
 
 
+def bwd(lib, q, k, v, do, **kw):
+    return oracle.sdpa_backward_reference(q, k, v, do, lib=lib, **kw)
+
+
+def pin_bwd_finite_differences(lib):
+    # central differences of the forward oracle: d/dX sum(dO * O(Q, K, V)),
+    # independent of every formula in the backward routine
+    B, Hq, Hkv, S, D = 1, 2, 1, 5, 3
+    q, k, v, do = rnd(80, B, S, Hq, D), rnd(81, B, S, Hkv, D), rnd(82, B, S, Hkv, D), rnd(83, B, S, Hq, D)
+    for causal in (False, True):
+        dq, dk, dv = bwd(lib, q, k, v, do, causal=causal, scale=0.9, dtype="f64")
+
+        def loss(q_, k_, v_):
+            return float((ref(lib, q_, k_, v_, causal=causal, scale=0.9, dtype="f64") * do).sum())
+
+        h = 1e-6
+        for x, g, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(*x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p, args_m = [q, k, v], [q, k, v]
+                args_p[which], args_m[which] = xp, xm
+                num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            np.testing.assert_allclose(g, num, rtol=1e-6, atol=1e-8)
+
+
+def pin_bwd_torch_autograd(lib):
+    # torch's float64 autograd of scaled_dot_product_attention, GQA by
+    # repeating K and V (their gradients sum over each group)
+    B, Hq, Hkv, Sq, Skv, D = 2, 4, 2, 9, 11, 8
+    q, k, v, do = rnd(84, B, Sq, Hq, D), rnd(85, B, Skv, Hkv, D), rnd(86, B, Skv, Hkv, D), rnd(87, B, Sq, Hq, D)
+    for causal in (False, True):
+        dq, dk, dv = bwd(lib, q, k, v, do, causal=causal, scale=0.4, dtype="f64")
+        qt = torch.tensor(q).transpose(1, 2).requires_grad_()
+        kt = torch.tensor(k).transpose(1, 2).requires_grad_()
+        vt = torch.tensor(v).transpose(1, 2).requires_grad_()
+        kr, vr = kt.repeat_interleave(2, dim=1), vt.repeat_interleave(2, dim=1)
+        mask = torch.ones(Sq, Skv, dtype=torch.bool).tril() if causal else None
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kr, vr, attn_mask=mask, scale=0.4)
+        o.backward(torch.tensor(do).transpose(1, 2))
+        np.testing.assert_allclose(dq, qt.grad.transpose(1, 2).numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dk, kt.grad.transpose(1, 2).numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dv, vt.grad.transpose(1, 2).numpy(), rtol=0, atol=1e-12)
+
+
+def pin_bwd_closed_forms(lib):
+    # constant V: O is constant in Q and K, so dQ = dK = 0 and dV_j = sum of
+    # the weights times dO; one key: the softmax is 1, so dQ = dK = 0 and
+    # dV = sum over rows (and grouped heads) of dO
+    q, k, do = rnd(88, 1, 6, 2, 4), rnd(89, 1, 7, 1, 4), rnd(90, 1, 6, 2, 4)
+    v = np.full((1, 7, 1, 4), 2.5)
+    dq, dk, _ = bwd(lib, q, k, v, do, causal=True, dtype="f64")
+    np.testing.assert_allclose(dq, 0, atol=1e-14)
+    np.testing.assert_allclose(dk, 0, atol=1e-14)
+    k1, v1 = rnd(91, 1, 1, 1, 4), rnd(92, 1, 1, 1, 4)
+    dq, dk, dv = bwd(lib, q, k1, v1, do, causal=False, dtype="f64")
+    np.testing.assert_allclose(dq, 0, atol=1e-14)
+    np.testing.assert_allclose(dk, 0, atol=1e-14)
+    np.testing.assert_allclose(dv[0, 0, 0], do.sum(axis=(0, 1, 2)), rtol=0, atol=1e-13)
+
+
 PINS = [pin_hand_cases, pin_single_key, pin_constant_v, pin_zero_query_is_mean,
         pin_causal_first_and_last_rows, pin_causal_rows_are_prefix_attention,
         pin_gqa_equals_repeated_mha, pin_key_permutation_invariance, pin_key_shift_invariance,
         pin_dominant_key_large_logits, pin_weights_rows_sum_to_one, pin_torch_sdpa_float64,
-        pin_e4m3_descales, pin_lse_closed_forms, pin_lse_scipy_logsumexp]
+        pin_e4m3_descales, pin_lse_closed_forms, pin_lse_scipy_logsumexp, pin_bwd_finite_differences,
+        pin_bwd_torch_autograd, pin_bwd_closed_forms]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -334,6 +398,12 @@ MUTANTS = {
     "fp16_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
     "lse_without_max": ("*lse_out = m + log(denom);", "*lse_out = log(denom);"),
     "lse_in_log2": ("*lse_out = m + log(denom);", "*lse_out = m + log2(denom);"),
+    "bwd_causal_sees_next_key": ("? i + 1 : Skv;", "? i + 2 : Skv;"),
+    "bwd_no_delta": ("const double dS = P[j] * (dP[j] - mean);", "const double dS = P[j] * dP[j];"),
+    "bwd_dk_unscaled": ("dk[d] += scale * dS *", "dk[d] += dS *"),
+    "bwd_dv_uses_ds": ("dv[d] += P[j] * load_elem(dO,", "dv[d] += dS * load_elem(dO,"),
+    "bwd_dq_reads_v": ("dq[d] += scale * dS * load_elem(K, bshd(b, j, g, d,",
+                       "dq[d] += scale * dS * load_elem(V, bshd(b, j, g, d,"),
 }
 
 
