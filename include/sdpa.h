@@ -199,6 +199,28 @@ sdpa_status_t sdpa_fwd_decode_noalloc(const void *Q, const void *K, const void *
                                       float scale, sdpa_dtype_t dtype, void *stream);
 
 /*
+ * Backward pass (bf16 / fp16, contiguous BSHD, D 64 or 128): the gradients of
+ * sum(dO * O) for O = sdpa_fwd(Q, K, V) with the same scale and mask.
+ *   Q, K, V   the forward's inputs; O its output; dO the upstream gradient
+ *             (shaped and typed like O); LSE the forward's log-sum-exp
+ *             (fp32 [B][Hq][Sq], from sdpa_fwd_ex).  All device, read only.
+ *   dQ        device, written, like Q; dK, dV device, written, like K.
+ *   workspace device scratch of at least sdpa_bwd_workspace_bytes(B, Hq,
+ *             Sq, D) bytes, 16-byte aligned, needing no initialisation, not
+ *             used by a concurrent call.
+ * Written buffers must not overlap one another or any input.  P is rounded
+ * to 16 bits before dV = P^T dO, dS before dK and dQ; accumulation is fp32.
+ */
+sdpa_status_t sdpa_bwd(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                       const float *LSE, void *dQ, void *dK, void *dV,
+                       int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                       float scale, int causal, sdpa_dtype_t dtype,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes sdpa_bwd needs (0 for invalid sizes). */
+size_t sdpa_bwd_workspace_bytes(int B, int Hq, int Sq, int D);
+
+/*
  * Workspace bytes sdpa_fwd_decode needs for this shape on the current device
  * (0: no split, or invalid sizes).  Initialises the library on the current
  * device on first use.
@@ -219,7 +241,8 @@ int sdpa_last_cuda_error(void);
  */
 sdpa_status_t sdpa_device_error(unsigned int *code);
 
-/* Version of this ABI (bumped on any change; 2 added the *_ex entry points, 3 the decode pass). */
+/* Version of this ABI (bumped on any change; 2 added the *_ex entry points, 3 the decode pass,
+ * 4 the backward pass). */
 int sdpa_abi_version(void);
 
 #ifdef __cplusplus

@@ -15,6 +15,7 @@ from . import _abi
 from ._abi import SdpaError, check, lib, status_string
 
 __all__ = ["sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_fwd_decode", "sdpa_fwd_decode_noalloc",
+           "sdpa_bwd", "bwd_workspace_bytes",
            "decode_workspace_bytes", "sdpa_status_string", "sdpa_device_error", "SdpaError", "lib"]
 
 _DTYPE = {torch.bfloat16: _abi.SDPA_DTYPE_BF16, torch.float16: _abi.SDPA_DTYPE_FP16}
@@ -207,6 +208,43 @@ def sdpa_fwd_decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o
                                         ctypes.byref(lk), ctypes.byref(lv), ctypes.byref(lo), float(scale),
                                         _DTYPE.get(q.dtype, 99), _stream_ptr(stream, q.device.index)))
     return o
+
+
+def bwd_workspace_bytes(B: int, Hq: int, Sq: int, D: int) -> int:
+    """Workspace bytes :func:`sdpa_bwd` needs."""
+    return int(lib().sdpa_bwd_workspace_bytes(B, Hq, Sq, D))
+
+
+def sdpa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, *, causal: bool = False, scale: float | None = None,
+             workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of sum(do * o) for o = sdpa_fwd(q, k, v) on
+    contiguous [B, S, H, D] bf16 / fp16 CUDA tensors; ``lse`` is the
+    forward's [B, Hq, Sq] float32 log-sum-exp (from :func:`sdpa_fwd_ex`).
+    Outputs and the workspace are allocated when not given."""
+    for t in (q, k, v, o, do):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError("q, k, v, o, do must be contiguous CUDA tensors of one dtype")
+    B, Hq, Hkv, Sq, Skv, D = _shapes(q, k, v)
+    if tuple(o.shape) != tuple(q.shape) or tuple(do.shape) != tuple(q.shape) or tuple(k.shape) != tuple(v.shape):
+        raise ValueError("o and do must be shaped like q, v like k")
+    lse_ptr = _lse_ptr(lse, B, Hq, Sq)
+    if lse_ptr is None:
+        raise ValueError("the forward's lse is required")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, like in ((dq, q), (dk, k), (dv, v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != like.dtype or t.shape != like.shape:
+            raise ValueError("gradients must be contiguous CUDA tensors shaped and typed like their inputs")
+    if workspace is None:
+        workspace = torch.empty(bwd_workspace_bytes(B, Hq, Sq, D), dtype=torch.uint8, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    check(lib().sdpa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse_ptr,
+                         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
+                         int(bool(causal)), _DTYPE.get(q.dtype, 99), workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), _stream_ptr(stream, q.device.index)))
+    return dq, dk, dv
 
 
 def sdpa_status_string(status: int) -> str:

@@ -14,7 +14,7 @@ STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_NULL_PTR", 2: "SDPA_ERR_MISALIGNED", 3: "SD
           12: "SDPA_ERR_WORKSPACE"}
 # every function include/sdpa.h declares
 EXPORTS = ("sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_fwd_decode",
-           "sdpa_fwd_decode_noalloc", "sdpa_decode_workspace_bytes", "sdpa_status_string", "sdpa_last_cuda_error", "sdpa_device_error",
+           "sdpa_fwd_decode_noalloc", "sdpa_decode_workspace_bytes", "sdpa_bwd", "sdpa_bwd_workspace_bytes", "sdpa_status_string", "sdpa_last_cuda_error", "sdpa_device_error",
            "sdpa_abi_version")
 
 
@@ -48,6 +48,10 @@ def _bind(lib):
     lib.sdpa_fwd_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, lp, lp, lp, lp, f, i, vp, ctypes.c_size_t, vp]
     lib.sdpa_fwd_decode_noalloc.restype = i
     lib.sdpa_fwd_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, lp, lp, lp, lp, f, i, vp]
+    lib.sdpa_bwd.restype = i
+    lib.sdpa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, vp]
+    lib.sdpa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.sdpa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.sdpa_decode_workspace_bytes.restype = ctypes.c_size_t
     lib.sdpa_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
     lib.sdpa_status_string.restype = ctypes.c_char_p

@@ -14,6 +14,7 @@
 
 #include "../../include/sdpa.h"
 #include "sdpa_kernel.cuh"
+#include "sdpa_bwd.cuh"
 
 namespace {
 
@@ -72,6 +73,13 @@ cudaError_t set_attrs()
                                 sdpa::Layout<D, KIND>::kSmemBytes);
 }
 
+template <int D, int KIND>
+cudaError_t set_bwd_attrs()
+{
+    return cudaFuncSetAttribute(sdpa::bwd::sdpa_bwd_kernel<D, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                sdpa::bwd::BwdLayout<D>::kSmemBytes);
+}
+
 sdpa_status_t device_ready(int* dev_out, int* sm_count)
 {
     int dev = 0;
@@ -103,7 +111,9 @@ sdpa_status_t device_ready(int* dev_out, int* sm_count)
                             set_attrs<128, sdpa::kFP16>(),       set_attrs<128, sdpa::kE4M3>(),
                             set_attrs<32, sdpa::kBF16, true>(),  set_attrs<32, sdpa::kFP16, true>(),
                             set_attrs<64, sdpa::kBF16, true>(),  set_attrs<64, sdpa::kFP16, true>(),
-                            set_attrs<128, sdpa::kBF16, true>(), set_attrs<128, sdpa::kFP16, true>()};
+                            set_attrs<128, sdpa::kBF16, true>(), set_attrs<128, sdpa::kFP16, true>(),
+                            set_bwd_attrs<64, sdpa::kBF16>(),    set_bwd_attrs<64, sdpa::kFP16>(),
+                            set_bwd_attrs<128, sdpa::kBF16>(),   set_bwd_attrs<128, sdpa::kFP16>()};
         for (cudaError_t x : es)
             if (x != cudaSuccess && st.err == cudaSuccess)
                 st.err = x;
@@ -541,6 +551,114 @@ sdpa_status_t run_decode(const Args& a, float scale, sdpa_dtype_t dtype, void* w
     return SDPA_OK;
 }
 
+// Backward pass workspace: the fp32 dQ accumulator [B][Sq][Hq][D], then
+// Delta [B][Hq][Sq].
+size_t bwd_workspace(int B, int Hq, int Sq, int D)
+{
+    return static_cast<size_t>(B) * Sq * Hq * D * sizeof(float) + static_cast<size_t>(B) * Hq * Sq * sizeof(float);
+}
+
+template <int D, int KIND>
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                       const sdpa::bwd::Params& p, const void* O, const void* dO, void* dQ, cudaStream_t stream)
+{
+    constexpr bool kBF16 = (KIND == sdpa::kBF16);
+    const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
+    cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(float), stream);
+    if (e != cudaSuccess)
+        return e;
+    sdpa::bwd::bwd_delta_kernel<D, kBF16><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
+        O, dO, const_cast<float*>(p.delta), p.B, p.Hq, p.Sq);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.n_kt);
+    sdpa::bwd::sdpa_bwd_kernel<D, KIND>
+        <<<grid, sdpa::bwd::kThreads, sdpa::bwd::BwdLayout<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    const long long n = rows * D;
+    sdpa::bwd::bwd_dq_convert_kernel<kBF16><<<static_cast<unsigned>((n / 4 + 255) / 256), 256, 0, stream>>>(
+        p.dq_acc, dQ, n);
+    return cudaGetLastError();
+}
+
+sdpa_status_t run_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                      void* dQ, void* dK, void* dV, const Shape& s, float scale, int causal, sdpa_dtype_t dtype,
+                      void* ws, size_t ws_bytes, void* stream)
+{
+    if (dtype != SDPA_DTYPE_BF16 && dtype != SDPA_DTYPE_FP16)
+        return SDPA_ERR_DTYPE;
+    const Args fwd{Q, K, V, dQ, nullptr, s, contiguous_bshd(s.Sq, s.Hq, s.D), contiguous_bshd(s.Skv, s.Hkv, s.D),
+                   contiguous_bshd(s.Skv, s.Hkv, s.D), contiguous_bshd(s.Sq, s.Hq, s.D)};
+    if (!O || !dO || !LSE || !dK || !dV || !ws)
+        return SDPA_ERR_NULL_PTR;
+    sdpa_status_t st = check_common(fwd, 2, 2);      // Q, K, V, dQ: pointers, sizes, heads, dQ vs inputs
+    if (st != SDPA_OK)
+        return st;
+    if (s.D != 64 && s.D != 128)
+        return SDPA_ERR_HEAD_DIM;
+    if (!aligned16(O) || !aligned16(dO) || !aligned16(dK) || !aligned16(dV) || !aligned16(ws) || !aligned(LSE, 4))
+        return SDPA_ERR_MISALIGNED;
+    if (!valid_scale(scale))
+        return SDPA_ERR_SCALE;
+    if (ws_bytes < bwd_workspace(s.B, s.Hq, s.Sq, s.D))
+        return SDPA_ERR_WORKSPACE;
+    const long long q_b = static_cast<long long>(s.B) * s.Sq * s.Hq * s.D * 2;
+    const long long kv_b = static_cast<long long>(s.B) * s.Skv * s.Hkv * s.D * 2;
+    const long long l_b = static_cast<long long>(s.B) * s.Hq * s.Sq * 4;
+    const long long w_b = static_cast<long long>(bwd_workspace(s.B, s.Hq, s.Sq, s.D));
+    // every written buffer (dQ, dK, dV, workspace) apart from every other buffer
+    const void* bufs[10] = {Q, K, V, O, dO, LSE, dQ, dK, dV, ws};
+    const long long lens[10] = {q_b, kv_b, kv_b, q_b, q_b, l_b, q_b, kv_b, kv_b, w_b};
+    for (int w = 6; w < 10; ++w)
+        for (int o = 0; o < 10; ++o)
+            if (o != w && overlaps(bufs[w], lens[w], bufs[o], lens[o]))
+                return SDPA_ERR_ALIAS;
+
+    int dev = 0, sm_count = 0;
+    st = device_ready(&dev, &sm_count);
+    if (st != SDPA_OK)
+        return st;
+    const CUtensorMapDataType dt =
+        dtype == SDPA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_map(&tq, Q, dt, 2, s.D, s.Hq, s.Sq, s.B, fwd.q) || !make_map(&tk, K, dt, 2, s.D, s.Hkv, s.Skv, s.B, fwd.k) ||
+        !make_map(&tv, V, dt, 2, s.D, s.Hkv, s.Skv, s.B, fwd.v) ||
+        !make_map(&tdo, dO, dt, 2, s.D, s.Hq, s.Sq, s.B, fwd.q))
+        return cuda_fail(cudaErrorInvalidValue);
+
+    sdpa::bwd::Params p{};
+    p.lse = LSE;
+    p.dq_acc = static_cast<float*>(ws);
+    p.delta = p.dq_acc + static_cast<long long>(s.B) * s.Sq * s.Hq * s.D;
+    p.dK = dK;
+    p.dV = dV;
+    p.B = s.B;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.Sq = s.Sq;
+    p.Skv = s.Skv;
+    p.group = s.Hq / s.Hkv;
+    p.n_qt = (s.Sq + sdpa::kBlockM - 1) / sdpa::kBlockM;
+    p.n_kt = (s.Skv + sdpa::kBlockN - 1) / sdpa::kBlockN;
+    p.causal = causal ? 1 : 0;
+    p.scale = scale;
+    p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
+    if (static_cast<long long>(s.B) * s.Hkv * p.n_kt > INT32_MAX)
+        return SDPA_ERR_BAD_SHAPE;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (dtype == SDPA_DTYPE_BF16)
+        e = s.D == 64 ? launch_bwd<64, sdpa::kBF16>(tq, tk, tv, tdo, p, O, dO, dQ, cs)
+                      : launch_bwd<128, sdpa::kBF16>(tq, tk, tv, tdo, p, O, dO, dQ, cs);
+    else
+        e = s.D == 64 ? launch_bwd<64, sdpa::kFP16>(tq, tk, tv, tdo, p, O, dO, dQ, cs)
+                      : launch_bwd<128, sdpa::kFP16>(tq, tk, tv, tdo, p, O, dO, dQ, cs);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    return SDPA_OK;
+}
+
 Args make_args(const void* Q, const void* K, const void* V, void* O, float* lse, int B, int Hq, int Hkv, int Sq,
                int Skv, int D, const sdpa_layout_t* ql, const sdpa_layout_t* kl, const sdpa_layout_t* vl,
                const sdpa_layout_t* ol)
@@ -624,6 +742,21 @@ sdpa_status_t sdpa_fwd_decode_noalloc(const void* Q, const void* K, const void* 
     return run_decode(a, scale, dtype, scratch, kDecodeScratchBytes, stream);
 }
 
+sdpa_status_t sdpa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                       void* dQ, void* dK, void* dV, int B, int Hq, int Hkv, int Sq, int Skv, int D, float scale,
+                       int causal, sdpa_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream)
+{
+    return run_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, Shape{B, Hq, Hkv, Sq, Skv, D}, scale, causal, dtype, workspace,
+                   workspace_bytes, stream);
+}
+
+size_t sdpa_bwd_workspace_bytes(int B, int Hq, int Sq, int D)
+{
+    if (B < 1 || Hq < 1 || Sq < 1 || (D != 64 && D != 128))
+        return 0;
+    return bwd_workspace(B, Hq, Sq, D);
+}
+
 size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int D)
 {
     if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Skv < 1 || Hq % Hkv != 0 || (D != 32 && D != 64 && D != 128))
@@ -680,7 +813,7 @@ sdpa_status_t sdpa_device_error(unsigned int* code)
 
 int sdpa_abi_version(void)
 {
-    return 3;
+    return 4;
 }
 
 }  // extern "C"

@@ -1,0 +1,475 @@
+// sdpa_bwd.cuh -- backward pass of the attention forward pass, for sm_103a.
+//
+// For O = softmax(S) V with S = scale Q K^T (the definition in section 1,
+// "How attention works", of the codelab "Attention on GPU (cuDNN and
+// TransformerEngine)") and an upstream gradient dO, the chain rule gives
+//     P = exp(S - LSE)                     (the forward's row log-sum-exp)
+//     dV = P^T dO,   dP = dO V^T,   Delta_i = sum_j P_ij dP_ij = dO_i . O_i
+//     dS = P * (dP - Delta),   dQ = scale dS K,   dK = scale dS^T Q.
+// The codelab names the backward pass as what training needs (section 10,
+// FP8: "E5M2 for the backward pass"); this is its bf16 / fp16 form.
+//
+// One CTA per (batch, KV head, key tile of 128 keys) owns dK and dV of its
+// keys and loops over the query tiles (causal: those on or below its keys)
+// of every query head of the group, accumulating in TMEM:
+//   warp 0       TMA producer: K, V once; Q and dO tiles into a 2-stage ring
+//   warp 1       tcgen05 issue, per query tile:
+//                  S^T = K Q^T (cols 0..127), dP^T = V dO^T (cols 128..255);
+//                  after the softmax: dV += P^T dO and dK += dS^T Q (P^T, dS^T
+//                  read from TMEM), dQ_part = dS K (dS from shared memory,
+//                  an MN-major A operand) into cols 0..D-1
+//   warps 4..7   one thread per key row: P^T = exp2(S^T c - LSE2), dS^T =
+//                  scale P^T (dP^T - Delta), written as 16-bit values over
+//                  S^T / dP^T in TMEM and, for dQ, to shared memory; at the
+//                  end dK, dV to HBM
+//   warps 8..11  one thread per query row: dQ_part from TMEM, added into an
+//                  fp32 dQ accumulator in HBM (vector atomics: every key tile
+//                  of the row contributes)
+// A preprocessing kernel forms Delta, a final one converts the fp32 dQ.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "sdpa_kernel.cuh"
+
+namespace sdpa {
+namespace bwd {
+
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kSoftmaxWarp0 = 4;     // warps 4..7
+constexpr int kDqWarp0 = 8;          // warps 8..11
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum : unsigned int {
+    kErrBwdWait = 0x400,             // + barrier id: a backward-pass wait timed out
+};
+
+struct Params {
+    const float* lse;                // [B][Hq][Sq] natural log-sum-exp of the forward
+    const float* delta;              // [B][Hq][Sq] dO_i . O_i
+    float* dq_acc;                   // [B][Sq][Hq][D] fp32, zero on entry
+    void* dK;                        // [B][Skv][Hkv][D] 16-bit
+    void* dV;
+    int B, Hq, Hkv, Sq, Skv, group;
+    int n_qt, n_kt;                  // query / key tiles of 128
+    int causal;
+    float scale;
+    float scale_log2;                // scale * log2(e)
+};
+
+// Shared memory: K, V (one tile each), Q and dO (two stages each), the dS^T
+// tile for dQ (keys x 128 queries, 16-bit, two 64-query chunks with the
+// 128-byte swizzle), barriers.
+template <int D>
+struct BwdLayout {
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kSwz = kRowBytes < 128 ? kRowBytes : 128;
+    static constexpr int kChunks = kRowBytes / kSwz;
+    static constexpr int kChunkBytes = kBlockM * kSwz;
+    static constexpr int kTileBytes = kBlockM * kRowBytes;
+    static constexpr int kSbo = 8 * kSwz;
+    static constexpr uint32_t kSwzCode = (kSwz == 128) ? 2u : 4u;
+    static constexpr int kSteps = kRowBytes / 32;                      // K = D MMAs: 16 elements each
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kTileBytes;
+    static constexpr int kOffQ = kOffV + kTileBytes;                  // 2 stages
+    static constexpr int kOffDO = kOffQ + 2 * kTileBytes;             // 2 stages
+    static constexpr int kOffDS = kOffDO + 2 * kTileBytes;            // 128 x 128 x 2 bytes
+    static constexpr int kDSChunkBytes = kBlockN * 128;               // 64 queries of every key row
+    static constexpr int kOffBar = kOffDS + 2 * kDSChunkBytes;
+    static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    static_assert(kColDK + D <= 512, "TMEM columns");
+};
+
+struct BwdBarriers {
+    uint64_t kv_full;
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
+    uint64_t s_full;
+    uint64_t p_full;
+    uint64_t dq_full;
+    uint64_t dq_free;
+    uint64_t dkv_full;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// The query tiles a CTA visits: for each head of its KV head's group, query
+// tiles qt0 .. n_qt-1 (causal: qt0 = the CTA's key tile, the first query
+// tile with a row that sees one of its keys; rows are top-left aligned).
+__device__ __forceinline__ int bwd_qt0(const Params& p, int kt)
+{
+    return p.causal ? kt : 0;
+}
+
+// Delta_i = dO_i . O_i (fp32), one warp per row (b, hq, i) of the
+// [B][Hq][Sq] layout; dO and O are [B][Sq][Hq][D] 16-bit.
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(128) bwd_delta_kernel(const void* O, const void* dO, float* delta, int B, int Hq,
+                                                       int Sq)
+{
+    const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= (int64_t)B * Hq * Sq)
+        return;
+    const int i = (int)(row % Sq);
+    const int64_t bh = row / Sq;
+    const int hq = (int)(bh % Hq);
+    const int b = (int)(bh / Hq);
+    const int64_t off = (((int64_t)b * Sq + i) * Hq + hq) * D;
+    float acc = 0.f;
+    for (int d = lane; d < D; d += 32) {
+        float o, g;
+        if constexpr (kBF16) {
+            o = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(O)[off + d]);
+            g = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(dO)[off + d]);
+        } else {
+            o = __half2float(reinterpret_cast<const __half*>(O)[off + d]);
+            g = __half2float(reinterpret_cast<const __half*>(dO)[off + d]);
+        }
+        acc += o * g;
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0)
+        delta[row] = acc;
+}
+
+// dQ (16-bit, [B][Sq][Hq][D]) from the fp32 accumulator, 4 elements a thread.
+template <bool kBF16>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* acc, void* dQ, int64_t n)
+{
+    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i >= n)
+        return;
+    const float4 v = *reinterpret_cast<const float4*>(acc + i);
+    uint2 out;
+    out.x = pack2<kBF16>(v.x, v.y);
+    out.y = pack2<kBF16>(v.z, v.w);
+    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(dQ) + i) = out;
+}
+
+template <int D, int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const Params p)
+{
+    using L = BwdLayout<D>;
+    constexpr bool kOutBF16 = (KIND == sdpa::kBF16);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    auto* bars = reinterpret_cast<BwdBarriers*>(smem + L::kOffBar);
+    volatile int* abort = &bars->abort;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // this CTA: key tile kt of KV head hkv of batch b
+    const int kt = blockIdx.x % p.n_kt;
+    const int bg = blockIdx.x / p.n_kt;
+    const int hkv = bg % p.Hkv;
+    const int b = bg / p.Hkv;
+    const int qt0 = bwd_qt0(p, kt);
+    const int n_q = p.n_qt > qt0 ? p.n_qt - qt0 : 0;
+    const int n_iter = n_q * p.group;            // (head, query tile) pairs, head-major
+
+    const uint32_t sK = smem_u32(smem + L::kOffK);
+    const uint32_t sV = smem_u32(smem + L::kOffV);
+    const uint32_t sQ = smem_u32(smem + L::kOffQ);
+    const uint32_t sDO = smem_u32(smem + L::kOffDO);
+    const uint32_t sDS = smem_u32(smem + L::kOffDS);
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars->kv_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&bars->q_full[s]), 1);
+            mbar_init(smem_u32(&bars->q_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&bars->s_full), 1);
+        mbar_init(smem_u32(&bars->p_full), 128);
+        mbar_init(smem_u32(&bars->dq_full), 1);
+        mbar_init(smem_u32(&bars->dq_free), 128);
+        mbar_init(smem_u32(&bars->dkv_full), 1);
+        mbar_init(smem_u32(&bars->drain), 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(&bars->tmem_base), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    auto head_of = [&](int it) { return hkv * p.group + it / n_q; };
+    auto qtile_of = [&](int it) { return qt0 + it % n_q; };
+
+    if (warp == kProducerWarp) {
+        // =========================== TMA producer ===========================
+        if (lane == 0 && n_iter > 0) {
+            tma_prefetch_map(&tm_q);
+            tma_prefetch_map(&tm_k);
+            tma_prefetch_map(&tm_v);
+            tma_prefetch_map(&tm_do);
+            constexpr int kCe = L::kSwz / 2;                       // elements per chunk
+            mbar_arrive_expect_tx(smem_u32(&bars->kv_full), 2 * L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c) {
+                tma_load_4d(sK + c * L::kChunkBytes, &tm_k, smem_u32(&bars->kv_full), c * kCe, hkv, kt * kBlockN, b);
+                tma_load_4d(sV + c * L::kChunkBytes, &tm_v, smem_u32(&bars->kv_full), c * kCe, hkv, kt * kBlockN, b);
+            }
+            int issued = 0;
+            for (int it = 0; it < n_iter; ++it) {
+                const int s = it & 1;
+                if (it >= 2 &&
+                    !wait_bar(smem_u32(&bars->q_empty[s]), ((it >> 1) & 1) ^ 1, abort, kErrBwdWait + 1))
+                    break;
+                const int h = head_of(it), qt = qtile_of(it);
+                mbar_arrive_expect_tx(smem_u32(&bars->q_full[s]), 2 * L::kTileBytes);
+                for (int c = 0; c < L::kChunks; ++c) {
+                    tma_load_4d(sQ + s * L::kTileBytes + c * L::kChunkBytes, &tm_q, smem_u32(&bars->q_full[s]),
+                                c * kCe, h, qt * kBlockM, b);
+                    tma_load_4d(sDO + s * L::kTileBytes + c * L::kChunkBytes, &tm_do, smem_u32(&bars->q_full[s]),
+                                c * kCe, h, qt * kBlockM, b);
+                }
+                ++issued;
+            }
+            if (*abort) {
+                // never leave the CTA with copies in flight
+                drain_wait(smem_u32(&bars->kv_full), 0);
+                for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
+                    drain_wait(smem_u32(&bars->q_full[it & 1]), (it >> 1) & 1);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ============================ MMA issuer ============================
+        if (lane == 0 && n_iter > 0) {
+            constexpr uint32_t kFmt = kOutBF16 ? 1u : 0u;
+            constexpr uint32_t id_s = idesc_make(kFmt, kBlockM, kBlockN, false);    // K-major A and B
+            constexpr uint32_t id_o = idesc_make(kFmt, kBlockM, D, true);           // A in TMEM, B MN-major
+            constexpr uint32_t id_q = idesc_make_amn(kFmt, kBlockM, D, true);       // A and B MN-major
+            // descriptors as (hi, lo) halves: K-major use of a tile (LBO unused)
+            // and MN-major use (LBO = the next 64-element chunk)
+            const uint32_t hi = (uint32_t)(smem_desc(0, 16, L::kSbo, L::kSwzCode) >> 32);
+            const uint32_t hi_ds = (uint32_t)(smem_desc(0, 16, 1024, 2u) >> 32);
+            const uint32_t kmaj = 1u << 16;
+            const uint32_t mnmaj = (uint32_t)(L::kChunkBytes >> 4) << 16;
+            const uint32_t k_lo = (sK >> 4) | kmaj, k_mn = (sK >> 4) | mnmaj;
+            const uint32_t v_lo = (sV >> 4) | kmaj;
+            const uint32_t ds_lo = (sDS >> 4) | ((uint32_t)(L::kDSChunkBytes >> 4) << 16);
+            const uint32_t s_t = tmem + L::kColS, dp_t = tmem + L::kColDP;
+            const uint32_t dv_t = tmem + L::kColDV, dk_t = tmem + L::kColDK;
+            bool ok = wait_bar(smem_u32(&bars->kv_full), 0, abort, kErrBwdWait + 2);
+            for (int it = 0; ok && it < n_iter; ++it) {
+                const int s = it & 1;
+                ok = wait_bar(smem_u32(&bars->q_full[s]), (it >> 1) & 1, abort, kErrBwdWait + 3);
+                if (ok && it > 0)        // the dQ warps have read the previous dQ_part out of cols 0..D-1
+                    ok = wait_bar(smem_u32(&bars->dq_free), (it - 1) & 1, abort, kErrBwdWait + 4);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                const uint32_t q_lo = ((sQ + s * L::kTileBytes) >> 4) | kmaj;
+                const uint32_t q_mn = ((sQ + s * L::kTileBytes) >> 4) | mnmaj;
+                const uint32_t do_lo = ((sDO + s * L::kTileBytes) >> 4) | kmaj;
+                const uint32_t do_mn = ((sDO + s * L::kTileBytes) >> 4) | mnmaj;
+                // S^T = K Q^T and dP^T = V dO^T (keys x queries), K = D
+#pragma unroll
+                for (int kk = 0; kk < L::kSteps; ++kk) {
+                    const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
+                    mma_f16_ss(s_t, desc_join(hi, k_lo + off), desc_join(hi, q_lo + off), id_s, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < L::kSteps; ++kk) {
+                    const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
+                    mma_f16_ss(dp_t, desc_join(hi, v_lo + off), desc_join(hi, do_lo + off), id_s, kk > 0);
+                }
+                mma_commit(smem_u32(&bars->s_full));
+                ok = wait_bar(smem_u32(&bars->p_full), it & 1, abort, kErrBwdWait + 5);
+                if (!ok)
+                    break;
+                tc_fence_after_sync();
+                // dV += P^T dO and dK += dS^T Q: 16 queries per step, P^T / dS^T
+                // from TMEM (8 columns per step), dO / Q MN-major
+#pragma unroll
+                for (int kk = 0; kk < kBlockM / 16; ++kk) {
+                    const uint32_t off = (uint32_t)((kk * 16 * L::kSwz) >> 4);
+                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                    mma_f16_ts(dv_t, s_t + kk * 8, desc_join(hi, do_mn + off), id_o, acc);
+                }
+#pragma unroll
+                for (int kk = 0; kk < kBlockM / 16; ++kk) {
+                    const uint32_t off = (uint32_t)((kk * 16 * L::kSwz) >> 4);
+                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                    mma_f16_ts(dk_t, dp_t + kk * 8, desc_join(hi, q_mn + off), id_o, acc);
+                }
+                // dQ_part = dS K: A = dS (queries x keys) from the dS^T tile read
+                // MN-major, 16 keys (rows of 128 bytes) per step; K MN-major.
+                // Issued after the P^T read above, so it may overwrite cols 0..D-1.
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                    const uint32_t off_a = (uint32_t)((kk * 16 * 128) >> 4);
+                    const uint32_t off_b = (uint32_t)((kk * 16 * L::kSwz) >> 4);
+                    mma_f16_ss(s_t, desc_join(hi_ds, ds_lo + off_a), desc_join(hi, k_mn + off_b), id_q, kk > 0);
+                }
+                mma_commit(smem_u32(&bars->q_empty[s]));
+                mma_commit(smem_u32(&bars->dq_full));
+            }
+            mma_commit(smem_u32(&bars->dkv_full));
+            mma_commit(smem_u32(&bars->drain));
+            drain_wait(smem_u32(&bars->drain), 0);
+        }
+    } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
+        // ==================== P^T and dS^T, one thread per key ===============
+        const int quarter = warp & 3;
+        const int kr = quarter * 32 + lane;                 // key row of the tile (= TMEM lane)
+        const int key = kt * kBlockN + kr;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const uint32_t s_t = tmem + lane_addr + L::kColS;
+        const uint32_t dp_t = tmem + lane_addr + L::kColDP;
+        const float c = p.scale_log2;
+        const bool key_ok = key < p.Skv;
+        bool ok = true;
+        for (int it = 0; ok && it < n_iter; ++it) {
+            const int h = head_of(it), qt = qtile_of(it);
+            const int64_t stat0 = ((int64_t)b * p.Hq + h) * p.Sq;
+            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full), it & 1, abort, kErrBwdWait + 6));
+            if (!ok)
+                break;
+            tc_fence_after_sync();
+            const int q_base = qt * kBlockM;
+            // top-left causal: this key is visible to query q iff key <= q
+            const int first_q = p.causal ? key - q_base : 0;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {                // 32 queries per chunk
+                // LSE (as log2) and Delta of the chunk's queries: lane l loads
+                // query 32ch + l, the others read it by shuffle; queries past
+                // Sq get LSE = +inf, so their weights are 0
+                const int qme = q_base + 32 * ch + lane;
+                const float lse2_me = qme < p.Sq ? p.lse[stat0 + qme] * kLog2e : INFINITY;
+                const float delta_me = qme < p.Sq ? p.delta[stat0 + qme] : 0.f;
+                uint32_t sv[32], dv[32];
+                tmem_ld32_wait(s_t + 32 * ch, sv);
+                tmem_ld32_wait(dp_t + 32 * ch, dv);
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int q0 = 32 * ch + 2 * i;
+                    float pr[2], ds[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int q = q0 + e;
+                        const bool vis = key_ok && q >= first_q;
+                        const float lse2 = __shfl_sync(0xffffffffu, lse2_me, 2 * i + e);
+                        const float delta = __shfl_sync(0xffffffffu, delta_me, 2 * i + e);
+                        const float pv = vis ? ex2_approx(__uint_as_float(sv[2 * i + e]) * c - lse2) : 0.f;
+                        pr[e] = pv;
+                        ds[e] = pv * (__uint_as_float(dv[2 * i + e]) - delta) * p.scale;
+                    }
+                    pk[i] = pack2<kOutBF16>(pr[0], pr[1]);
+                    dk[i] = pack2<kOutBF16>(ds[0], ds[1]);
+                }
+                tmem_st16(s_t + 16 * ch, pk);               // over S^T columns already read
+                tmem_st16(dp_t + 16 * ch, dk);
+                // dS^T row for dQ: queries 32ch .. 32ch+31 are 16-byte units
+                // 4(ch&1) .. +3 of 64-query chunk ch/2, 128-byte swizzle
+                const uint32_t row_base = sDS + (ch >> 1) * L::kDSChunkBytes + kr * 128;
+#pragma unroll
+                for (int uu = 0; uu < 4; ++uu) {
+                    const int u = 4 * (ch & 1) + uu;
+                    st_shared_v4(row_base + (uint32_t)((u ^ (kr & 7)) << 4), dk[4 * uu], dk[4 * uu + 1],
+                                 dk[4 * uu + 2], dk[4 * uu + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(smem_u32(&bars->p_full));
+        }
+        // ---- dK, dV of this key (dK carries the scale already, through dS) ----
+        // The wait and the TMEM loads are warp-wide (every lane takes part);
+        // only keys below Skv store.
+        if (ok && n_iter > 0) {
+            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->dkv_full), 0, abort, kErrBwdWait + 7));
+            tc_fence_after_sync();
+        }
+        if (ok) {
+            const int64_t row_off = (((int64_t)b * p.Skv + key) * p.Hkv + hkv) * D;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                uint16_t* dst = reinterpret_cast<uint16_t*>(which ? p.dK : p.dV) + row_off;
+                const uint32_t col = which ? L::kColDK : L::kColDV;
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t r[32];
+                    if (n_iter > 0) {
+                        tmem_ld32_wait(tmem + lane_addr + col + 32 * cc, r);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = 0u;                      // no query sees this key
+                    }
+                    if (key_ok) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            reinterpret_cast<uint4*>(dst + 32 * cc)[v] = make_uint4(
+                                pack2<kOutBF16>(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
+                                pack2<kOutBF16>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                                pack2<kOutBF16>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                                pack2<kOutBF16>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+                    }
+                }
+            }
+        }
+    } else if (warp >= kDqWarp0) {
+        // ================== dQ_part into the fp32 accumulator ================
+        const int quarter = warp & 3;
+        const int qr = quarter * 32 + lane;                 // query row of the tile (= TMEM lane)
+        const uint32_t src = tmem + ((uint32_t)(quarter * 32) << 16) + L::kColS;
+        bool ok = true;
+        for (int it = 0; ok && it < n_iter; ++it) {
+            const int h = head_of(it), qt = qtile_of(it);
+            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->dq_full), it & 1, abort, kErrBwdWait + 8));
+            if (!ok)
+                break;
+            tc_fence_after_sync();
+            uint32_t r[D];
+            if constexpr (D == 128) {
+                tmem_ld128_wait(src, src + 32, src + 64, src + 96, r);
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc)
+                    tmem_ld32_wait(src + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * cc]));
+            }
+            tc_fence_before_sync();
+            mbar_arrive(smem_u32(&bars->dq_free));
+            const int q = qt * kBlockM + qr;
+            if (q < p.Sq) {
+                float4* dst = reinterpret_cast<float4*>(p.dq_acc + (((int64_t)b * p.Sq + q) * p.Hq + h) * D);
+#pragma unroll
+                for (int v = 0; v < D / 4; ++v)
+                    atomicAdd(dst + v, make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace bwd
+}  // namespace sdpa
