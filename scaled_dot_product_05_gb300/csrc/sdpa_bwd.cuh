@@ -18,11 +18,13 @@
 //                  after the softmax: dV += P^T dO and dK += dS^T Q (P^T, dS^T
 //                  read from TMEM), dQ_part = dS K (dS from shared memory,
 //                  an MN-major A operand) into cols 0..D-1
-//   warps 4..7   one thread per key row: P^T = exp2(S^T c - LSE2), dS^T =
-//                  scale P^T (dP^T - Delta), written as 16-bit values over
-//                  S^T / dP^T in TMEM and, for dQ, to shared memory; at the
-//                  end dK, dV to HBM
-//   warps 8..11  one thread per query row: dQ_part from TMEM, added into an
+//   warps 4..11  two warpgroups, one thread per key row each, the first for
+//                  queries 0..63 of the tile, the second for 64..127:
+//                  P^T = exp2(S^T c - LSE2), dS^T = scale P^T (dP^T - Delta),
+//                  written as 16-bit values over S^T / dP^T in TMEM and, for
+//                  dQ, to shared memory; at the end dV (first) and dK
+//                  (second) to HBM
+//   warps 12..15 one thread per query row: dQ_part from TMEM, added into an
 //                  fp32 dQ accumulator in HBM (vector atomics: every key tile
 //                  of the row contributes)
 // A preprocessing kernel forms Delta, a final one converts the fp32 dQ.
@@ -39,11 +41,18 @@
 namespace sdpa {
 namespace bwd {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kSoftmaxWarp0 = 4;     // warps 4..7
-constexpr int kDqWarp0 = 8;          // warps 8..11
+constexpr int kSoftmaxWarp0 = 4;     // warps 4..11: two warpgroups, 64 queries each
+constexpr int kDqWarp0 = 12;         // warps 12..15
+// Register split: launched at 128 per thread (512 x 128 = 65536); warps 0..3
+// drop to 80, the two softmax warpgroups rise to 144, the dQ warpgroup keeps
+// 128: 128 x 80 + 256 x 144 + 128 x 128 = 63488 <= 65536 (the split with no
+// spills; 56 / 152 spilled).
+constexpr uint32_t kRegsLow = 80;
+constexpr uint32_t kRegsSoftmax = 144;
+static_assert(128 * kRegsLow + 256 * kRegsSoftmax + 128 * 128 <= kThreads * 128, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : unsigned int {
@@ -63,9 +72,24 @@ struct Params {
     float scale_log2;                // scale * log2(e)
 };
 
+struct BwdBarriers {
+    uint64_t kv_full;
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
+    uint64_t s_full;
+    uint64_t p_full;
+    uint64_t dq_full;
+    uint64_t dq_free;
+    uint64_t dkv_full;
+    uint64_t stats_full[2];          // LSE2 / Delta buffer written (count 128)
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
 // Shared memory: K, V (one tile each), Q and dO (two stages each), the dS^T
 // tile for dQ (keys x 128 queries, 16-bit, two 64-query chunks with the
-// 128-byte swizzle), barriers.
+// 128-byte swizzle), LSE2 / Delta of the query tile in two buffers, barriers.
 template <int D>
 struct BwdLayout {
     static constexpr int kRowBytes = D * 2;
@@ -82,26 +106,17 @@ struct BwdLayout {
     static constexpr int kOffDO = kOffQ + 2 * kTileBytes;             // 2 stages
     static constexpr int kOffDS = kOffDO + 2 * kTileBytes;            // 128 x 128 x 2 bytes
     static constexpr int kDSChunkBytes = kBlockN * 128;               // 64 queries of every key row
-    static constexpr int kOffBar = kOffDS + 2 * kDSChunkBytes;
-    static constexpr int kSmemBytes = kOffBar + 256 + 1024;
+    static constexpr int kOffStats = kOffDS + 2 * kDSChunkBytes;      // 2 x (LSE2[128], Delta[128])
+    static constexpr int kOffBar = kOffStats + 2 * 2 * kBlockM * 4;
+    // the dynamic shared memory is declared 1024-byte aligned (the 128-byte
+    // swizzle needs it), so no alignment slack is added
+    static constexpr int kSmemBytes = kOffBar + 128;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    static_assert(sizeof(BwdBarriers) <= 128, "barrier block");
     static_assert(kColDK + D <= 512, "TMEM columns");
 };
 
-struct BwdBarriers {
-    uint64_t kv_full;
-    uint64_t q_full[2];
-    uint64_t q_empty[2];
-    uint64_t s_full;
-    uint64_t p_full;
-    uint64_t dq_full;
-    uint64_t dq_free;
-    uint64_t dkv_full;
-    uint64_t drain;
-    uint32_t tmem_base;
-    int abort;
-};
 
 // The query tiles a CTA visits: for each head of its KV head's group, query
 // tiles qt0 .. n_qt-1 (causal: qt0 = the CTA's key tile, the first query
@@ -166,8 +181,14 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 {
     using L = BwdLayout<D>;
     constexpr bool kOutBF16 = (KIND == sdpa::kBF16);
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {
+        // the layout relies on the declared alignment; never seen otherwise
+        if (threadIdx.x == 0)
+            atomicCAS(&g_sdpa_error, 0u, kErrBwdWait + 15);
+        return;
+    }
+    uint8_t* smem = smem_raw;
     auto* bars = reinterpret_cast<BwdBarriers*>(smem + L::kOffBar);
     volatile int* abort = &bars->abort;
     const int warp = threadIdx.x >> 5;
@@ -187,6 +208,7 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t sQ = smem_u32(smem + L::kOffQ);
     const uint32_t sDO = smem_u32(smem + L::kOffDO);
     const uint32_t sDS = smem_u32(smem + L::kOffDS);
+    float* stats = reinterpret_cast<float*>(smem + L::kOffStats);      // [2][LSE2 128 | Delta 128]
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars->kv_full), 1);
@@ -195,10 +217,12 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(smem_u32(&bars->q_empty[s]), 1);
         }
         mbar_init(smem_u32(&bars->s_full), 1);
-        mbar_init(smem_u32(&bars->p_full), 128);
+        mbar_init(smem_u32(&bars->p_full), 256);           // both softmax warpgroups
         mbar_init(smem_u32(&bars->dq_full), 1);
         mbar_init(smem_u32(&bars->dq_free), 128);
         mbar_init(smem_u32(&bars->dkv_full), 1);
+        mbar_init(smem_u32(&bars->stats_full[0]), 128);
+        mbar_init(smem_u32(&bars->stats_full[1]), 128);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -214,7 +238,9 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     auto head_of = [&](int it) { return hkv * p.group + it / n_q; };
     auto qtile_of = [&](int it) { return qt0 + it % n_q; };
 
-    if (warp == kProducerWarp) {
+    if (warp < kSoftmaxWarp0) {
+      regs_release<kRegsLow>();
+      if (warp == kProducerWarp) {
         // =========================== TMA producer ===========================
         if (lane == 0 && n_iter > 0) {
             tma_prefetch_map(&tm_q);
@@ -298,18 +324,21 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     break;
                 tc_fence_after_sync();
                 // dV += P^T dO and dK += dS^T Q: 16 queries per step, P^T / dS^T
-                // from TMEM (8 columns per step), dO / Q MN-major
+                // from TMEM (8 columns per step: queries 0..63 in cols 0..31,
+                // 64..127 in cols 64..95), dO / Q MN-major
 #pragma unroll
                 for (int kk = 0; kk < kBlockM / 16; ++kk) {
                     const uint32_t off = (uint32_t)((kk * 16 * L::kSwz) >> 4);
                     const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                    mma_f16_ts(dv_t, s_t + kk * 8, desc_join(hi, do_mn + off), id_o, acc);
+                    const uint32_t col = (kk < 4) ? 8 * kk : 32 + 8 * kk;
+                    mma_f16_ts(dv_t, s_t + col, desc_join(hi, do_mn + off), id_o, acc);
                 }
 #pragma unroll
                 for (int kk = 0; kk < kBlockM / 16; ++kk) {
                     const uint32_t off = (uint32_t)((kk * 16 * L::kSwz) >> 4);
                     const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                    mma_f16_ts(dk_t, dp_t + kk * 8, desc_join(hi, q_mn + off), id_o, acc);
+                    const uint32_t col = (kk < 4) ? 8 * kk : 32 + 8 * kk;
+                    mma_f16_ts(dk_t, dp_t + col, desc_join(hi, q_mn + off), id_o, acc);
                 }
                 // dQ_part = dS K: A = dS (queries x keys) from the dS^T tile read
                 // MN-major, 16 keys (rows of 128 bytes) per step; K MN-major.
@@ -327,8 +356,11 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mma_commit(smem_u32(&bars->drain));
             drain_wait(smem_u32(&bars->drain), 0);
         }
-    } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
+      }
+    } else if (warp < kDqWarp0) {
+        regs_acquire<kRegsSoftmax>();
         // ==================== P^T and dS^T, one thread per key ===============
+        const int sw = (warp - kSoftmaxWarp0) >> 2;         // query half of this warpgroup
         const int quarter = warp & 3;
         const int kr = quarter * 32 + lane;                 // key row of the tile (= TMEM lane)
         const int key = kt * kBlockN + kr;
@@ -337,54 +369,76 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t dp_t = tmem + lane_addr + L::kColDP;
         const float c = p.scale_log2;
         const bool key_ok = key < p.Skv;
+        // LSE2 / Delta of query row kr of iteration `it` (+inf / 0 past Sq)
+        auto stat_of = [&](int it, float& l2, float& dl) {
+            const int qrow = qtile_of(it) * kBlockM + kr;
+            const int64_t at = ((int64_t)b * p.Hq + head_of(it)) * p.Sq + qrow;
+            l2 = qrow < p.Sq ? p.lse[at] * kLog2e : INFINITY;
+            dl = qrow < p.Sq ? p.delta[at] : 0.f;
+        };
+        // the first warpgroup keeps the statistics buffers
+        if (n_iter > 0 && sw == 0) {
+            float l2, dl;
+            stat_of(0, l2, dl);
+            stats[kr] = l2;
+            stats[kBlockM + kr] = dl;
+            mbar_arrive(smem_u32(&bars->stats_full[0]));
+        }
         bool ok = true;
         for (int it = 0; ok && it < n_iter; ++it) {
-            const int h = head_of(it), qt = qtile_of(it);
-            const int64_t stat0 = ((int64_t)b * p.Hq + h) * p.Sq;
             ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full), it & 1, abort, kErrBwdWait + 6));
+            // the next tile's LSE2 / Delta: loaded now, stored after this tile
+            float nl2 = 0.f, ndl = 0.f;
+            if (sw == 0 && it + 1 < n_iter)
+                stat_of(it + 1, nl2, ndl);
+            if (ok)
+                ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->stats_full[it & 1]), (it >> 1) & 1, abort,
+                                                      kErrBwdWait + 9));
             if (!ok)
                 break;
             tc_fence_after_sync();
-            const int q_base = qt * kBlockM;
-            // top-left causal: this key is visible to query q iff key <= q
-            const int first_q = p.causal ? key - q_base : 0;
+            const float4* l2v = reinterpret_cast<const float4*>(stats + (it & 1) * 2 * kBlockM);
+            const float4* dlv = l2v + kBlockM / 4;
+            // top-left causal: this key is visible to query q iff key <= q;
+            // keys past Skv are visible to none
+            const int first_q = !key_ok ? (1 << 30) : (p.causal ? key - qtile_of(it) * kBlockM : -1);
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {                // 32 queries per chunk
-                // LSE (as log2) and Delta of the chunk's queries: lane l loads
-                // query 32ch + l, the others read it by shuffle; queries past
-                // Sq get LSE = +inf, so their weights are 0
-                const int qme = q_base + 32 * ch + lane;
-                const float lse2_me = qme < p.Sq ? p.lse[stat0 + qme] * kLog2e : INFINITY;
-                const float delta_me = qme < p.Sq ? p.delta[stat0 + qme] : 0.f;
+            for (int chh = 0; chh < 2; ++chh) {             // 32 queries per chunk, two per warpgroup
+                const int ch = 2 * sw + chh;
                 uint32_t sv[32], dv[32];
                 tmem_ld32_wait(s_t + 32 * ch, sv);
                 tmem_ld32_wait(dp_t + 32 * ch, dv);
                 uint32_t pk[16], dk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int q0 = 32 * ch + 2 * i;
-                    float pr[2], ds[2];
+                for (int i = 0; i < 8; ++i) {
+                    const float4 l4 = l2v[8 * ch + i];
+                    const float4 d4 = dlv[8 * ch + i];
+                    const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const float dq[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pr[4], ds[4];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int q = q0 + e;
-                        const bool vis = key_ok && q >= first_q;
-                        const float lse2 = __shfl_sync(0xffffffffu, lse2_me, 2 * i + e);
-                        const float delta = __shfl_sync(0xffffffffu, delta_me, 2 * i + e);
-                        const float pv = vis ? ex2_approx(__uint_as_float(sv[2 * i + e]) * c - lse2) : 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        const int q = 32 * ch + 4 * i + e;
+                        const float pv = q >= first_q ? ex2_approx(__uint_as_float(sv[4 * i + e]) * c - lq[e]) : 0.f;
                         pr[e] = pv;
-                        ds[e] = pv * (__uint_as_float(dv[2 * i + e]) - delta) * p.scale;
+                        ds[e] = pv * p.scale * (__uint_as_float(dv[4 * i + e]) - dq[e]);
                     }
-                    pk[i] = pack2<kOutBF16>(pr[0], pr[1]);
-                    dk[i] = pack2<kOutBF16>(ds[0], ds[1]);
+                    pk[2 * i] = pack2<kOutBF16>(pr[0], pr[1]);
+                    pk[2 * i + 1] = pack2<kOutBF16>(pr[2], pr[3]);
+                    dk[2 * i] = pack2<kOutBF16>(ds[0], ds[1]);
+                    dk[2 * i + 1] = pack2<kOutBF16>(ds[2], ds[3]);
                 }
-                tmem_st16(s_t + 16 * ch, pk);               // over S^T columns already read
-                tmem_st16(dp_t + 16 * ch, dk);
+                // 16-bit values over this warpgroup's own S^T / dP^T columns,
+                // already read (the other warpgroup may not have read its own
+                // yet): queries 64 sw + 32 chh .. +31 in cols 64 sw + 16 chh ..
+                tmem_st16(s_t + 64 * sw + 16 * chh, pk);
+                tmem_st16(dp_t + 64 * sw + 16 * chh, dk);
                 // dS^T row for dQ: queries 32ch .. 32ch+31 are 16-byte units
-                // 4(ch&1) .. +3 of 64-query chunk ch/2, 128-byte swizzle
-                const uint32_t row_base = sDS + (ch >> 1) * L::kDSChunkBytes + kr * 128;
+                // 4(ch&1) .. +3 of 64-query chunk ch/2 (= sw), 128-byte swizzle
+                const uint32_t row_base = sDS + sw * L::kDSChunkBytes + kr * 128;
 #pragma unroll
                 for (int uu = 0; uu < 4; ++uu) {
-                    const int u = 4 * (ch & 1) + uu;
+                    const int u = 4 * chh + uu;
                     st_shared_v4(row_base + (uint32_t)((u ^ (kr & 7)) << 4), dk[4 * uu], dk[4 * uu + 1],
                                  dk[4 * uu + 2], dk[4 * uu + 3]);
                 }
@@ -393,6 +447,14 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(smem_u32(&bars->p_full));
+            // the next tile's statistics into the other buffer: its last
+            // readers (tile it - 1) finished before this tile's S was issued
+            if (sw == 0 && it + 1 < n_iter) {
+                float* nb = stats + ((it + 1) & 1) * 2 * kBlockM;
+                nb[kr] = nl2;
+                nb[kBlockM + kr] = ndl;
+                mbar_arrive(smem_u32(&bars->stats_full[(it + 1) & 1]));
+            }
         }
         // ---- dK, dV of this key (dK carries the scale already, through dS) ----
         // The wait and the TMEM loads are warp-wide (every lane takes part);
@@ -403,8 +465,8 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         if (ok) {
             const int64_t row_off = (((int64_t)b * p.Skv + key) * p.Hkv + hkv) * D;
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
+            {
+                const int which = sw;                       // first warpgroup dV, second dK
                 uint16_t* dst = reinterpret_cast<uint16_t*>(which ? p.dK : p.dV) + row_off;
                 const uint32_t col = which ? L::kColDK : L::kColDV;
 #pragma unroll
@@ -441,23 +503,27 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!ok)
                 break;
             tc_fence_after_sync();
-            uint32_t r[D];
-            if constexpr (D == 128) {
-                tmem_ld128_wait(src, src + 32, src + 64, src + 96, r);
-            } else {
-#pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc)
-                    tmem_ld32_wait(src + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * cc]));
-            }
-            tc_fence_before_sync();
-            mbar_arrive(smem_u32(&bars->dq_free));
+            // D / 2 columns at a time; the TMEM read ends before the second
+            // half's atomics, which then overlap the next tile's S and dP
             const int q = qt * kBlockM + qr;
-            if (q < p.Sq) {
-                float4* dst = reinterpret_cast<float4*>(p.dq_acc + (((int64_t)b * p.Sq + q) * p.Hq + h) * D);
+            float4* dst = reinterpret_cast<float4*>(p.dq_acc + (((int64_t)b * p.Sq + q) * p.Hq + h) * D);
 #pragma unroll
-                for (int v = 0; v < D / 4; ++v)
-                    atomicAdd(dst + v, make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[D / 2];
+#pragma unroll
+                for (int cc = 0; cc < D / 64; ++cc)
+                    tmem_ld32_wait(src + half * (D / 2) + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * cc]));
+                if (half == 1) {
+                    tc_fence_before_sync();
+                    mbar_arrive(smem_u32(&bars->dq_free));
+                }
+                if (q < p.Sq) {
+#pragma unroll
+                    for (int v = 0; v < D / 8; ++v)
+                        atomicAdd(dst + half * (D / 8) + v,
+                                  make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+                }
             }
         }
     }
