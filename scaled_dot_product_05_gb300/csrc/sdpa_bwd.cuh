@@ -47,12 +47,12 @@ constexpr int kMmaWarp = 1;
 constexpr int kSoftmaxWarp0 = 4;     // warps 4..11: two warpgroups, 64 queries each
 constexpr int kDqWarp0 = 12;         // warps 12..15
 // Register split: launched at 128 per thread (512 x 128 = 65536); warps 0..3
-// drop to 80, the two softmax warpgroups rise to 144, the dQ warpgroup keeps
-// 128: 128 x 80 + 256 x 144 + 128 x 128 = 63488 <= 65536 (the split with no
-// spills; 56 / 152 spilled).
+// drop to 80, the two softmax warpgroups and the dQ warpgroup rise to 144:
+// 128 x 80 + 384 x 144 = 65536 (56 / 152 spilled).
 constexpr uint32_t kRegsLow = 80;
 constexpr uint32_t kRegsSoftmax = 144;
-static_assert(128 * kRegsLow + 256 * kRegsSoftmax + 128 * 128 <= kThreads * 128, "register split");
+constexpr uint32_t kRegsDq = 144;
+static_assert(128 * kRegsLow + 256 * kRegsSoftmax + 128 * kRegsDq <= kThreads * 128, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : unsigned int {
@@ -492,6 +492,7 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
     } else if (warp >= kDqWarp0) {
+        regs_acquire<kRegsDq>();
         // ================== dQ_part into the fp32 accumulator ================
         const int quarter = warp & 3;
         const int qr = quarter * 32 + lane;                 // query row of the tile (= TMEM lane)
@@ -503,27 +504,25 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!ok)
                 break;
             tc_fence_after_sync();
-            // D / 2 columns at a time; the TMEM read ends before the second
-            // half's atomics, which then overlap the next tile's S and dP
+            // all D columns out of TMEM first, so the next tile's S and dP can
+            // overwrite them while the atomics run
+            uint32_t r[D];
+            if constexpr (D == 128) {
+                tmem_ld128_wait(src, src + 32, src + 64, src + 96, r);
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc)
+                    tmem_ld32_wait(src + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * cc]));
+            }
+            tc_fence_before_sync();
+            mbar_arrive(smem_u32(&bars->dq_free));
             const int q = qt * kBlockM + qr;
-            float4* dst = reinterpret_cast<float4*>(p.dq_acc + (((int64_t)b * p.Sq + q) * p.Hq + h) * D);
+            if (q < p.Sq) {
+                float4* dst = reinterpret_cast<float4*>(p.dq_acc + (((int64_t)b * p.Sq + q) * p.Hq + h) * D);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t r[D / 2];
-#pragma unroll
-                for (int cc = 0; cc < D / 64; ++cc)
-                    tmem_ld32_wait(src + half * (D / 2) + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * cc]));
-                if (half == 1) {
-                    tc_fence_before_sync();
-                    mbar_arrive(smem_u32(&bars->dq_free));
-                }
-                if (q < p.Sq) {
-#pragma unroll
-                    for (int v = 0; v < D / 8; ++v)
-                        atomicAdd(dst + half * (D / 8) + v,
-                                  make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
-                }
+                for (int v = 0; v < D / 4; ++v)
+                    atomicAdd(dst + v, make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
             }
         }
     }
