@@ -54,6 +54,10 @@ DECODE_WORKLOADS = {
     "decode-gqa-b8-32k": (8, 32, 8, 1, 32768, 128),
     "decode-gqa-b32-8k": (32, 32, 8, 4, 8192, 128),
 }
+# backward pass (gradients of sum(dO * O)): name -> (B, Hq, Hkv, S, D, causal)
+BWD_WORKLOADS = {
+    "bwd-gqa-causal-4096": (2, 32, 8, 4096, 128, True),
+}
 DEFAULT_WORKLOAD = "gqa-causal-4096"
 
 
@@ -66,6 +70,9 @@ class Spec(tuple):
 
 
 def spec(name):
+    if name in BWD_WORKLOADS:
+        B, Hq, Hkv, S, D, causal = BWD_WORKLOADS[name]
+        return Spec((B, Hq, Hkv, S, S, D, causal, "bf16", False))
     if name in DECODE_WORKLOADS:
         B, Hq, Hkv, Sq, Skv, D = DECODE_WORKLOADS[name]
         return Spec((B, Hq, Hkv, Sq, Skv, D, False, "bf16", True))
@@ -73,7 +80,7 @@ def spec(name):
     return Spec((B, Hq, Hkv, S, S, D, causal, dtype, False))
 
 
-ALL_WORKLOADS = sorted(list(WORKLOADS) + list(DECODE_WORKLOADS))
+ALL_WORKLOADS = sorted(list(WORKLOADS) + list(DECODE_WORKLOADS) + list(BWD_WORKLOADS))
 
 
 def describe(name):
@@ -85,15 +92,19 @@ def describe(name):
 
 
 def step_flops(name):
-    """4 D FLOPs per visible score (causal: the lower triangle, Sq = Skv)."""
+    """4 D FLOPs per visible score (causal: the lower triangle, Sq = Skv);
+    the backward pass's five products (S, dP, dV, dK, dQ) are 10 D."""
     w = spec(name)
-    f = 4.0 * w.B * w.Hq * w.Sq * w.Skv * w.D
+    f = (10.0 if name in BWD_WORKLOADS else 4.0) * w.B * w.Hq * w.Sq * w.Skv * w.D
     return f / 2 if w.causal else f
 
 
 def step_bytes(name):
-    """Algorithmic bytes: Q, K, V read once and O written once."""
+    """Algorithmic bytes: Q, K, V read once and O written once (backward:
+    Q, K, V, O, dO and the LSE read, dQ, dK, dV written)."""
     w = spec(name)
+    if name in BWD_WORKLOADS:
+        return 2 * w.B * w.D * (3 * w.Sq * w.Hq + 4 * w.Skv * w.Hkv) + 4 * w.B * w.Hq * w.Sq
     e_in = 1 if w.dtype == "e4m3" else 2
     return w.B * w.D * (w.Sq * w.Hq * e_in + 2 * w.Skv * w.Hkv * e_in + w.Sq * w.Hq * 2)
 
@@ -264,10 +275,16 @@ def run_reference(args, rank, world):
     per_step_target = max(1.0, min(20.0, 90.0 / max(1, args.steps + args.warmup)))
     values = []
     desc, cores = "", 0
-    for i in range(args.warmup + args.steps):
-        tf, cores, desc = oracle_sample(name, seconds_target=per_step_target)
-        if i >= args.warmup:
-            values.append(tf)
+    if name in BWD_WORKLOADS:
+        # one bounded sample of the backward oracle (several seconds) stands
+        # for every step
+        tf, cores, desc = oracle_bwd_sample(name)
+        values = [tf]
+    else:
+        for i in range(args.warmup + args.steps):
+            tf, cores, desc = oracle_sample(name, seconds_target=per_step_target)
+            if i >= args.warmup:
+                values.append(tf)
     value = statistics.median(values)
     ms = step_flops(name) / (value * 1e12) * 1e3
     line = {
@@ -525,6 +542,144 @@ def run_gpu(args, rank, world, local_rank):
     return 0
 
 
+def oracle_bwd_sample(name, threads=0):
+    """Time the fp64 backward oracle on a bounded sample of the workload:
+    batch 0, every KV head (the oracle runs one thread per KV head), the
+    first 1024 positions; returns (TFLOP/s, threads, description)."""
+    import oracle
+    from sdpa_inputs import make_qkv
+
+    w = spec(name)
+    S = min(w.Sq, 1024)
+    x = make_qkv(1000, 1, w.Hq, w.Hkv, S, S, w.D, "bf16")
+    do = make_qkv(1001, 1, w.Hq, w.Hkv, S, S, w.D, "bf16").q
+    t0 = time.perf_counter()
+    oracle.sdpa_backward_reference(x.q, x.k, x.v, do, causal=w.causal, dtype="bf16", threads=threads)
+    dt = time.perf_counter() - t0
+    f = 10.0 * w.Hq * S * S * w.D * (0.5 if w.causal else 1.0)
+    return f / dt / 1e12, oracle.last_threads(), (
+        f"batch 0, all {w.Hkv} KV heads, positions 0..{S - 1} of the workload: {f / 1e9:.1f} GFLOP in {dt:.1f} s")
+
+
+def run_gpu_bwd(args, rank, world, local_rank):
+    """The backward pass: one step is sdpa_bwd on resident Q, K, V, O, dO and
+    the forward's LSE (rotating input sets, as for the forward)."""
+    import torch
+    import torch.distributed as dist
+
+    from scaled_dot_product_05_gb300 import bwd_workspace_bytes, sdpa_bwd, sdpa_device_error, sdpa_fwd_ex
+    from sdpa_inputs import make_qkv
+
+    name = args.workload
+    w = spec(name)
+    B, Hq, Hkv, S, D, causal = w.B, w.Hq, w.Hkv, w.Sq, w.D, w.causal
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    n_sets = n_rotating_sets(name)
+    sets = []
+    host = None
+    for i in range(n_sets):
+        x = make_qkv(100 + 17 * rank + i, B, Hq, Hkv, S, S, D, "bf16")
+        do = make_qkv(200 + 17 * rank + i, B, Hq, Hkv, S, S, D, "bf16").q
+        q, k, v, g = (t.to(dev) for t in (x.q, x.k, x.v, do))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+        sdpa_fwd_ex(q, k, v, o, lse, causal=causal)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        sets.append((q, k, v, o, g, lse, grads))
+        if i == 0:
+            host = tuple(t.cpu().pin_memory() for t in (q, k, v, o, g, lse))
+    ws = torch.empty(bwd_workspace_bytes(B, Hq, S, D), dtype=torch.uint8, device=dev)
+
+    def launch(i, st=None):
+        q, k, v, o, g, lse, (dq, dk, dv) = sets[i % n_sets]
+        sdpa_bwd(q, k, v, o, g, lse, dq, dk, dv, causal=causal, workspace=ws, stream=st or stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        launch(i)
+    barrier()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        launch(i)
+    end.record(stream)
+    barrier()
+    ms_per_step = max_over_ranks(start.elapsed_time(end), world, dev) / args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        launch(i)
+        ev[i][1].record(stream)
+    barrier()
+    t_wall1 = time.time()
+    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    err = sdpa_device_error()
+    if err:
+        raise RuntimeError(f"device error word 0x{err:x}")
+    # end to end: inputs copied in from pinned host memory, gradients copied
+    # out, every step (serial on the launching stream)
+    hq_, hk_, hv_, ho_, hg_, hl_ = host
+    out_host = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in sets[0][6])
+    bi = sum(t.numel() * t.element_size() for t in host)
+    bo = sum(t.numel() * t.element_size() for t in out_host)
+    q, k, v, o, g, lse, grads = sets[0]
+    e2e_steps = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for dst, src in zip((q, k, v, o, g, lse), host):
+            dst.copy_(src, non_blocking=True)
+        launch(0)
+        for dst, src in zip(out_host, grads):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    if sampler:
+        sampler.stop()
+    if rank != 0:
+        return 0
+
+    flops = step_flops(name)
+    peaks, peak_src = load_peaks()
+    avg_kernel_ms = statistics.mean(kern_ms)
+    achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": whole_job_tflops(flops, world, ms_per_step), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), inputs resident in HBM)",
+        "config": {"workload": "backward pass, " + describe(name), "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": S, "Skv": S,
+                   "D": D, "causal": causal, "flops_per_step": flops, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 ({n_sets} rotating input sets of {step_bytes(name) / 1e6:.1f} MB)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": None, "peak_source": f"bf16 burst ({peak_src})", "kernel": "sdpa_bwd_kernel (+ Delta, "
+                     "dQ conversion; launch duration of the whole call)",
+                     "algorithmic_bytes_per_launch": step_bytes(name)},
+        "e2e": {"value": whole_job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms, "pipelined": "no (serial copy in, pass, copy out)"},
+        "gpu_launches": 2 * args.steps * 3,
+        "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        tf, cores, desc = oracle_bwd_sample(name)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -549,6 +704,8 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
+        if args.workload in BWD_WORKLOADS:
+            return run_gpu_bwd(args, rank, world, local_rank)
         return run_gpu(args, rank, world, local_rank)
     finally:
         if world > 1:
