@@ -560,7 +560,8 @@ size_t bwd_workspace(int B, int Hq, int Sq, int D)
 
 template <int D, int KIND>
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                       const sdpa::bwd::Params& p, const void* O, const void* dO, void* dQ, cudaStream_t stream)
+                       const CUtensorMap& tdq, const sdpa::bwd::Params& p, const void* O, const void* dO, void* dQ,
+                       cudaStream_t stream)
 {
     constexpr bool kBF16 = (KIND == sdpa::kBF16);
     const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
@@ -573,7 +574,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
         return e;
     const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.n_kt);
     sdpa::bwd::sdpa_bwd_kernel<D, KIND>
-        <<<grid, sdpa::bwd::kThreads, sdpa::bwd::BwdLayout<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+        <<<grid, sdpa::bwd::kThreads, sdpa::bwd::BwdLayout<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
     const long long n = rows * D;
@@ -621,15 +622,19 @@ sdpa_status_t run_bwd(const void* Q, const void* K, const void* V, const void* O
         return st;
     const CUtensorMapDataType dt =
         dtype == SDPA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap tq, tk, tv, tdo;
+    // the fp32 dQ accumulator [B][Sq][Hq][D] at the start of the workspace
+    // takes TMA reductions: boxes of 32 columns x 128 rows, 128-byte swizzle
+    float* dq_acc = static_cast<float*>(ws);
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_map(&tq, Q, dt, 2, s.D, s.Hq, s.Sq, s.B, fwd.q) || !make_map(&tk, K, dt, 2, s.D, s.Hkv, s.Skv, s.B, fwd.k) ||
         !make_map(&tv, V, dt, 2, s.D, s.Hkv, s.Skv, s.B, fwd.v) ||
-        !make_map(&tdo, dO, dt, 2, s.D, s.Hq, s.Sq, s.B, fwd.q))
+        !make_map(&tdo, dO, dt, 2, s.D, s.Hq, s.Sq, s.B, fwd.q) ||
+        !make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.D, s.Hq, s.Sq, s.B, fwd.q))
         return cuda_fail(cudaErrorInvalidValue);
 
     sdpa::bwd::Params p{};
     p.lse = LSE;
-    p.dq_acc = static_cast<float*>(ws);
+    p.dq_acc = dq_acc;
     p.delta = p.dq_acc + static_cast<long long>(s.B) * s.Sq * s.Hq * s.D;
     p.dK = dK;
     p.dV = dV;
@@ -649,11 +654,11 @@ sdpa_status_t run_bwd(const void* Q, const void* K, const void* V, const void* O
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (dtype == SDPA_DTYPE_BF16)
-        e = s.D == 64 ? launch_bwd<64, sdpa::kBF16>(tq, tk, tv, tdo, p, O, dO, dQ, cs)
-                      : launch_bwd<128, sdpa::kBF16>(tq, tk, tv, tdo, p, O, dO, dQ, cs);
+        e = s.D == 64 ? launch_bwd<64, sdpa::kBF16>(tq, tk, tv, tdo, tdq, p, O, dO, dQ, cs)
+                      : launch_bwd<128, sdpa::kBF16>(tq, tk, tv, tdo, tdq, p, O, dO, dQ, cs);
     else
-        e = s.D == 64 ? launch_bwd<64, sdpa::kFP16>(tq, tk, tv, tdo, p, O, dO, dQ, cs)
-                      : launch_bwd<128, sdpa::kFP16>(tq, tk, tv, tdo, p, O, dO, dQ, cs);
+        e = s.D == 64 ? launch_bwd<64, sdpa::kFP16>(tq, tk, tv, tdo, tdq, p, O, dO, dQ, cs)
+                      : launch_bwd<128, sdpa::kFP16>(tq, tk, tv, tdo, tdq, p, O, dO, dQ, cs);
     if (e != cudaSuccess)
         return cuda_fail(e);
     return SDPA_OK;

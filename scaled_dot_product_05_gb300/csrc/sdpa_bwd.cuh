@@ -13,20 +13,22 @@
 // keys and loops over the query tiles (causal: those on or below its keys)
 // of every query head of the group, accumulating in TMEM:
 //   warp 0       TMA producer: K, V once; Q and dO tiles into a 2-stage ring
-//   warp 1       tcgen05 issue, per query tile:
-//                  S^T = K Q^T (cols 0..127), dP^T = V dO^T (cols 128..255);
-//                  after the softmax: dV += P^T dO and dK += dS^T Q (P^T, dS^T
-//                  read from TMEM), dQ_part = dS K (dS from shared memory,
-//                  an MN-major A operand) into cols 0..D-1
+//   warp 1       tcgen05 issue, per query tile: S^T = K Q^T (cols 0..127),
+//                  dP^T = V dO^T (cols 128..255); dV += P^T dO once P^T is
+//                  packed, dK += dS^T Q once dS^T is (both read from TMEM);
+//                  dQ_part = dS K (dS from shared memory, an MN-major A
+//                  operand) into cols 128..128+D-1, so the next tile's S^T
+//                  needs no wait for the dQ warps
 //   warps 4..11  two warpgroups, one thread per key row each, the first for
-//                  queries 0..63 of the tile, the second for 64..127:
-//                  P^T = exp2(S^T c - LSE2), dS^T = scale P^T (dP^T - Delta),
-//                  written as 16-bit values over S^T / dP^T in TMEM and, for
-//                  dQ, to shared memory; at the end dV (first) and dK
-//                  (second) to HBM
-//   warps 12..15 one thread per query row: dQ_part from TMEM, added into an
-//                  fp32 dQ accumulator in HBM (vector atomics: every key tile
-//                  of the row contributes)
+//                  queries 0..63 of the tile, the second for 64..127: first
+//                  P^T = exp2(S^T c - LSE2) (from S^T alone), then dS^T =
+//                  scale P^T (dP^T - Delta), each written as 16-bit values
+//                  over S^T / dP^T in TMEM, dS^T also to shared memory for
+//                  dQ; at the end dV (first) and dK (second) to HBM
+//   warps 12..15 one thread per query row: dQ_part from TMEM, staged in
+//                  shared memory (over the dS^T tile, once the dQ MMA has read
+//                  it) and added into an fp32 dQ accumulator in HBM by TMA
+//                  reductions (every key tile of a row contributes)
 // A preprocessing kernel forms Delta, a final one converts the fp32 dQ.
 #pragma once
 
@@ -76,12 +78,17 @@ struct BwdBarriers {
     uint64_t kv_full;
     uint64_t q_full[2];
     uint64_t q_empty[2];
-    uint64_t s_full;
-    uint64_t p_full;
+    uint64_t s_full;                 // S^T in TMEM
+    uint64_t dp_full;                // dP^T in TMEM
+    uint64_t p_ready;                // P^T packed in TMEM (both softmax warpgroups)
+    uint64_t ds_ready;               // dS^T packed in TMEM and shared memory
     uint64_t dq_full;
     uint64_t dq_free;
     uint64_t dkv_full;
     uint64_t stats_full[2];          // LSE2 / Delta buffer written (count 128)
+    uint64_t dstage_full;            // dQ_part slice staged in shared memory (count 128)
+    uint64_t dstage_read;            // the TMA reduction has read the staged slice
+    uint64_t dstage_free;            // the dS^T tile is free again (dQ of the tile reduced)
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -110,10 +117,10 @@ struct BwdLayout {
     static constexpr int kOffBar = kOffStats + 2 * 2 * kBlockM * 4;
     // the dynamic shared memory is declared 1024-byte aligned (the 128-byte
     // swizzle needs it), so no alignment slack is added
-    static constexpr int kSmemBytes = kOffBar + 128;
+    static constexpr int kSmemBytes = kOffBar + 256;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-    static_assert(sizeof(BwdBarriers) <= 128, "barrier block");
+    static_assert(sizeof(BwdBarriers) <= 256, "barrier block");
     static_assert(kColDK + D <= 512, "TMEM columns");
 };
 
@@ -177,7 +184,8 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* acc, v
 template <int D, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do, const Params p)
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_dq, const Params p)
 {
     using L = BwdLayout<D>;
     constexpr bool kOutBF16 = (KIND == sdpa::kBF16);
@@ -217,12 +225,17 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(smem_u32(&bars->q_empty[s]), 1);
         }
         mbar_init(smem_u32(&bars->s_full), 1);
-        mbar_init(smem_u32(&bars->p_full), 256);           // both softmax warpgroups
+        mbar_init(smem_u32(&bars->dp_full), 1);
+        mbar_init(smem_u32(&bars->p_ready), 256);          // both softmax warpgroups
+        mbar_init(smem_u32(&bars->ds_ready), 256);
         mbar_init(smem_u32(&bars->dq_full), 1);
         mbar_init(smem_u32(&bars->dq_free), 128);
         mbar_init(smem_u32(&bars->dkv_full), 1);
         mbar_init(smem_u32(&bars->stats_full[0]), 128);
         mbar_init(smem_u32(&bars->stats_full[1]), 128);
+        mbar_init(smem_u32(&bars->dstage_full), 128);
+        mbar_init(smem_u32(&bars->dstage_read), 1);
+        mbar_init(smem_u32(&bars->dstage_free), 1);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -298,8 +311,6 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int it = 0; ok && it < n_iter; ++it) {
                 const int s = it & 1;
                 ok = wait_bar(smem_u32(&bars->q_full[s]), (it >> 1) & 1, abort, kErrBwdWait + 3);
-                if (ok && it > 0)        // the dQ warps have read the previous dQ_part out of cols 0..D-1
-                    ok = wait_bar(smem_u32(&bars->dq_free), (it - 1) & 1, abort, kErrBwdWait + 4);
                 if (!ok)
                     break;
                 tc_fence_after_sync();
@@ -307,25 +318,31 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint32_t q_mn = ((sQ + s * L::kTileBytes) >> 4) | mnmaj;
                 const uint32_t do_lo = ((sDO + s * L::kTileBytes) >> 4) | kmaj;
                 const uint32_t do_mn = ((sDO + s * L::kTileBytes) >> 4) | mnmaj;
-                // S^T = K Q^T and dP^T = V dO^T (keys x queries), K = D
+                // S^T = K Q^T (keys x queries, K = D) into cols 0..127: the last
+                // tile's P^T there was read by its dV MMA, issued before this one
 #pragma unroll
                 for (int kk = 0; kk < L::kSteps; ++kk) {
                     const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
                     mma_f16_ss(s_t, desc_join(hi, k_lo + off), desc_join(hi, q_lo + off), id_s, kk > 0);
                 }
+                mma_commit(smem_u32(&bars->s_full));
+                // dP^T = V dO^T into cols 128..255, once the dQ warps have read the
+                // last tile's dQ_part out of them
+                if (it > 0 && !(ok = wait_bar(smem_u32(&bars->dq_free), (it - 1) & 1, abort, kErrBwdWait + 4)))
+                    break;
+                tc_fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < L::kSteps; ++kk) {
                     const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
                     mma_f16_ss(dp_t, desc_join(hi, v_lo + off), desc_join(hi, do_lo + off), id_s, kk > 0);
                 }
-                mma_commit(smem_u32(&bars->s_full));
-                ok = wait_bar(smem_u32(&bars->p_full), it & 1, abort, kErrBwdWait + 5);
-                if (!ok)
+                mma_commit(smem_u32(&bars->dp_full));
+                // dV += P^T dO as soon as P^T is packed: 16 queries per step, P^T
+                // from TMEM (8 columns per step: queries 0..63 in cols 0..31,
+                // 64..127 in cols 64..95), dO MN-major
+                if (!(ok = wait_bar(smem_u32(&bars->p_ready), it & 1, abort, kErrBwdWait + 5)))
                     break;
                 tc_fence_after_sync();
-                // dV += P^T dO and dK += dS^T Q: 16 queries per step, P^T / dS^T
-                // from TMEM (8 columns per step: queries 0..63 in cols 0..31,
-                // 64..127 in cols 64..95), dO / Q MN-major
 #pragma unroll
                 for (int kk = 0; kk < kBlockM / 16; ++kk) {
                     const uint32_t off = (uint32_t)((kk * 16 * L::kSwz) >> 4);
@@ -333,6 +350,10 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const uint32_t col = (kk < 4) ? 8 * kk : 32 + 8 * kk;
                     mma_f16_ts(dv_t, s_t + col, desc_join(hi, do_mn + off), id_o, acc);
                 }
+                // dK += dS^T Q, dS^T from TMEM like P^T; Q MN-major
+                if (!(ok = wait_bar(smem_u32(&bars->ds_ready), it & 1, abort, kErrBwdWait + 10)))
+                    break;
+                tc_fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < kBlockM / 16; ++kk) {
                     const uint32_t off = (uint32_t)((kk * 16 * L::kSwz) >> 4);
@@ -342,12 +363,12 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 // dQ_part = dS K: A = dS (queries x keys) from the dS^T tile read
                 // MN-major, 16 keys (rows of 128 bytes) per step; K MN-major.
-                // Issued after the P^T read above, so it may overwrite cols 0..D-1.
+                // Into cols 128..128+D-1: issued after the dK MMA read dS^T there.
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk) {
                     const uint32_t off_a = (uint32_t)((kk * 16 * 128) >> 4);
                     const uint32_t off_b = (uint32_t)((kk * 16 * L::kSwz) >> 4);
-                    mma_f16_ss(s_t, desc_join(hi_ds, ds_lo + off_a), desc_join(hi, k_mn + off_b), id_q, kk > 0);
+                    mma_f16_ss(dp_t, desc_join(hi_ds, ds_lo + off_a), desc_join(hi, k_mn + off_b), id_q, kk > 0);
                 }
                 mma_commit(smem_u32(&bars->q_empty[s]));
                 mma_commit(smem_u32(&bars->dq_full));
@@ -402,36 +423,62 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // top-left causal: this key is visible to query q iff key <= q;
             // keys past Skv are visible to none
             const int first_q = !key_ok ? (1 << 30) : (p.causal ? key - qtile_of(it) * kBlockM : -1);
+            // phase 1, from S^T alone: P^T, packed over this warpgroup's own
+            // S^T columns (already read; the other warpgroup may not have read
+            // its own yet): queries 64 sw + 32 chh .. +31 in cols 64 sw + 16 chh ..
+            float pf[2][32];
 #pragma unroll
             for (int chh = 0; chh < 2; ++chh) {             // 32 queries per chunk, two per warpgroup
                 const int ch = 2 * sw + chh;
-                uint32_t sv[32], dv[32];
+                uint32_t sv[32];
                 tmem_ld32_wait(s_t + 32 * ch, sv);
-                tmem_ld32_wait(dp_t + 32 * ch, dv);
-                uint32_t pk[16], dk[16];
+                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float4 l4 = l2v[8 * ch + i];
-                    const float4 d4 = dlv[8 * ch + i];
                     const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dq[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pr[4], ds[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int q = 32 * ch + 4 * i + e;
-                        const float pv = q >= first_q ? ex2_approx(__uint_as_float(sv[4 * i + e]) * c - lq[e]) : 0.f;
-                        pr[e] = pv;
-                        ds[e] = pv * p.scale * (__uint_as_float(dv[4 * i + e]) - dq[e]);
+                        pf[chh][4 * i + e] =
+                            q >= first_q ? ex2_approx(__uint_as_float(sv[4 * i + e]) * c - lq[e]) : 0.f;
                     }
-                    pk[2 * i] = pack2<kOutBF16>(pr[0], pr[1]);
-                    pk[2 * i + 1] = pack2<kOutBF16>(pr[2], pr[3]);
+                    pk[2 * i] = pack2<kOutBF16>(pf[chh][4 * i], pf[chh][4 * i + 1]);
+                    pk[2 * i + 1] = pack2<kOutBF16>(pf[chh][4 * i + 2], pf[chh][4 * i + 3]);
+                }
+                tmem_st16(s_t + 64 * sw + 16 * chh, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(smem_u32(&bars->p_ready));          // dV += P^T dO can start
+            // phase 2, once dP^T is there: dS^T = scale P^T (dP^T - Delta),
+            // packed over the warpgroup's own dP^T columns and into the
+            // shared tile for dQ
+            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->dp_full), it & 1, abort, kErrBwdWait + 11));
+            // the dS^T tile doubles as the dQ staging buffer of the last tile
+            if (ok && it > 0)
+                ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->dstage_free), (it - 1) & 1, abort,
+                                                      kErrBwdWait + 12));
+            if (!ok)
+                break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int chh = 0; chh < 2; ++chh) {
+                const int ch = 2 * sw + chh;
+                uint32_t dv[32];
+                tmem_ld32_wait(dp_t + 32 * ch, dv);
+                uint32_t dk[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 d4 = dlv[8 * ch + i];
+                    const float dq[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float ds[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        ds[e] = pf[chh][4 * i + e] * p.scale * (__uint_as_float(dv[4 * i + e]) - dq[e]);
                     dk[2 * i] = pack2<kOutBF16>(ds[0], ds[1]);
                     dk[2 * i + 1] = pack2<kOutBF16>(ds[2], ds[3]);
                 }
-                // 16-bit values over this warpgroup's own S^T / dP^T columns,
-                // already read (the other warpgroup may not have read its own
-                // yet): queries 64 sw + 32 chh .. +31 in cols 64 sw + 16 chh ..
-                tmem_st16(s_t + 64 * sw + 16 * chh, pk);
                 tmem_st16(dp_t + 64 * sw + 16 * chh, dk);
                 // dS^T row for dQ: queries 32ch .. 32ch+31 are 16-byte units
                 // 4(ch&1) .. +3 of 64-query chunk ch/2 (= sw), 128-byte swizzle
@@ -446,9 +493,10 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before_sync();
-            mbar_arrive(smem_u32(&bars->p_full));
+            mbar_arrive(smem_u32(&bars->ds_ready));
             // the next tile's statistics into the other buffer: its last
-            // readers (tile it - 1) finished before this tile's S was issued
+            // readers (tile it - 1, both phases) finished before that tile's
+            // ds_ready, which came before this tile's S was issued
             if (sw == 0 && it + 1 < n_iter) {
                 float* nb = stats + ((it + 1) & 1) * 2 * kBlockM;
                 nb[kr] = nl2;
@@ -496,7 +544,7 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // ================== dQ_part into the fp32 accumulator ================
         const int quarter = warp & 3;
         const int qr = quarter * 32 + lane;                 // query row of the tile (= TMEM lane)
-        const uint32_t src = tmem + ((uint32_t)(quarter * 32) << 16) + L::kColS;
+        const uint32_t src = tmem + ((uint32_t)(quarter * 32) << 16) + L::kColDP;   // dQ_part
         bool ok = true;
         for (int it = 0; ok && it < n_iter; ++it) {
             const int h = head_of(it), qt = qtile_of(it);
@@ -504,29 +552,54 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!ok)
                 break;
             tc_fence_after_sync();
-            // all D columns out of TMEM first, so the next tile's S and dP can
-            // overwrite them while the atomics run
+            // all D columns out of TMEM first, so the next tile's dP MMA can
+            // take the columns while this tile's dQ is reduced into HBM
             uint32_t r[D];
-            if constexpr (D == 128) {
-                tmem_ld128_wait(src, src + 32, src + 64, src + 96, r);
-            } else {
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc)
-                    tmem_ld32_wait(src + 32 * cc, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * cc]));
-            }
+            for (int c = 0; c < D / 32; ++c)
+                tmem_ld32_wait(src + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
             tc_fence_before_sync();
             mbar_arrive(smem_u32(&bars->dq_free));
-            const int q = qt * kBlockM + qr;
-            if (q < p.Sq) {
-                float4* dst = reinterpret_cast<float4*>(p.dq_acc + (((int64_t)b * p.Sq + q) * p.Hq + h) * D);
+            // into the fp32 accumulator by TMA reductions: 32-column slices
+            // (128 rows x 128 bytes, 128-byte swizzle) staged in the dS^T
+            // tile, two slices per round
 #pragma unroll
-                for (int v = 0; v < D / 4; ++v)
-                    atomicAdd(dst + v, make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+            for (int hh = 0; hh < D / 64; ++hh) {
+#pragma unroll
+                for (int box = 0; box < 2; ++box) {
+                    const uint32_t row = sDS + box * L::kDSChunkBytes + qr * 128;
+                    const int c0 = 64 * hh + 32 * box;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(row + (uint32_t)((u ^ (qr & 7)) << 4), r[c0 + 4 * u], r[c0 + 4 * u + 1],
+                                     r[c0 + 4 * u + 2], r[c0 + 4 * u + 3]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&bars->dstage_full));
+                const uint32_t round = (uint32_t)(it * (D / 64) + hh);
+                if (threadIdx.x == kDqWarp0 * 32) {
+                    if (wait_bar(smem_u32(&bars->dstage_full), round & 1, abort, kErrBwdWait + 13)) {
+                        for (int box = 0; box < 2; ++box)
+                            tma_reduce_add_4d(&tm_dq, sDS + box * L::kDSChunkBytes, 64 * hh + 32 * box, h,
+                                              qt * kBlockM, b);
+                        bulk_commit_group();
+                        bulk_wait_group_read0();            // the staging buffer may be overwritten
+                    }
+                    mbar_arrive(smem_u32(&bars->dstage_read));
+                }
+                __syncwarp();
+                ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->dstage_read), round & 1, abort,
+                                                      kErrBwdWait + 14));
+                if (!ok)
+                    break;
             }
+            if (ok && threadIdx.x == kDqWarp0 * 32)
+                mbar_arrive(smem_u32(&bars->dstage_free));
         }
     }
 
+    if (threadIdx.x == kDqWarp0 * 32)
+        bulk_wait_group0();                                 // the reductions have landed
     tc_fence_before_sync();
     __syncthreads();
     if (warp == kMmaWarp) {
