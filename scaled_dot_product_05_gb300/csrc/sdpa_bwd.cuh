@@ -13,6 +13,9 @@
 // keys and loops over the query tiles (causal: those on or below its keys)
 // of every query head of the group, accumulating in TMEM:
 //   warp 0       TMA producer: K, V once; Q and dO tiles into a 2-stage ring
+//   warp 2       dQ reducer: adds the staged dQ_part of a query tile into
+//                  the fp32 dQ accumulator in HBM (TMA bulk reductions), then
+//                  hands the tile's Q / dO stage back to the producer
 //   warp 1       tcgen05 issue, per query tile: S^T = K Q^T (cols 0..127),
 //                  dP^T = V dO^T (cols 128..255); dV += P^T dO once P^T is
 //                  packed, dK += dS^T Q once dS^T is (both read from TMEM);
@@ -26,9 +29,10 @@
 //                  over S^T / dP^T in TMEM, dS^T also to shared memory for
 //                  dQ; at the end dV (first) and dK (second) to HBM
 //   warps 12..15 one thread per query row: dQ_part from TMEM, staged in
-//                  shared memory (over the dS^T tile, once the dQ MMA has read
-//                  it) and added into an fp32 dQ accumulator in HBM by TMA
-//                  reductions (every key tile of a row contributes)
+//                  shared memory over the tile's Q and dO (every MMA that
+//                  reads them precedes the dQ MMA; 128 x D fp32 is exactly
+//                  their size), for the reducer (every key tile of a query
+//                  row contributes to its dQ)
 // A preprocessing kernel forms Delta, a final one converts the fp32 dQ.
 #pragma once
 
@@ -46,6 +50,7 @@ namespace bwd {
 constexpr int kThreads = 512;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
+constexpr int kReduceWarp = 2;
 constexpr int kSoftmaxWarp0 = 4;     // warps 4..11: two warpgroups, 64 queries each
 constexpr int kDqWarp0 = 12;         // warps 12..15
 // Register split: launched at 128 per thread (512 x 128 = 65536); warps 0..3
@@ -56,6 +61,7 @@ constexpr uint32_t kRegsSoftmax = 144;
 constexpr uint32_t kRegsDq = 144;
 static_assert(128 * kRegsLow + 256 * kRegsSoftmax + 128 * kRegsDq <= kThreads * 128, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kSliceBytes = kBlockM * 128;   // 32 fp32 columns of a 128-row dQ tile
 
 enum : unsigned int {
     kErrBwdWait = 0x400,             // + barrier id: a backward-pass wait timed out
@@ -86,9 +92,7 @@ struct BwdBarriers {
     uint64_t dq_free;
     uint64_t dkv_full;
     uint64_t stats_full[2];          // LSE2 / Delta buffer written (count 128)
-    uint64_t dstage_full;            // dQ_part slice staged in shared memory (count 128)
-    uint64_t dstage_read;            // the TMA reduction has read the staged slice
-    uint64_t dstage_free;            // the dS^T tile is free again (dQ of the tile reduced)
+    uint64_t dstage_full[2];         // dQ_part staged over Q / dO stage s (count 128)
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -202,9 +206,13 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // this CTA: key tile kt of KV head hkv of batch b
-    const int kt = blockIdx.x % p.n_kt;
-    const int bg = blockIdx.x / p.n_kt;
+    // this CTA: key tile kt of KV head hkv of batch b; key tiles in
+    // ascending order over the grid, so under the causal mask the CTAs with
+    // the most query tiles start first (longest first keeps the last wave
+    // short)
+    const int n_bg = p.B * p.Hkv;
+    const int kt = blockIdx.x / n_bg;
+    const int bg = blockIdx.x % n_bg;
     const int hkv = bg % p.Hkv;
     const int b = bg / p.Hkv;
     const int qt0 = bwd_qt0(p, kt);
@@ -233,9 +241,8 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(smem_u32(&bars->dkv_full), 1);
         mbar_init(smem_u32(&bars->stats_full[0]), 128);
         mbar_init(smem_u32(&bars->stats_full[1]), 128);
-        mbar_init(smem_u32(&bars->dstage_full), 128);
-        mbar_init(smem_u32(&bars->dstage_read), 1);
-        mbar_init(smem_u32(&bars->dstage_free), 1);
+        mbar_init(smem_u32(&bars->dstage_full[0]), 128);
+        mbar_init(smem_u32(&bars->dstage_full[1]), 128);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -370,12 +377,32 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const uint32_t off_b = (uint32_t)((kk * 16 * L::kSwz) >> 4);
                     mma_f16_ss(dp_t, desc_join(hi_ds, ds_lo + off_a), desc_join(hi, k_mn + off_b), id_q, kk > 0);
                 }
-                mma_commit(smem_u32(&bars->q_empty[s]));
-                mma_commit(smem_u32(&bars->dq_full));
+                mma_commit(smem_u32(&bars->dq_full));       // also frees Q / dO stage s for dQ staging
             }
             mma_commit(smem_u32(&bars->dkv_full));
             mma_commit(smem_u32(&bars->drain));
             drain_wait(smem_u32(&bars->drain), 0);
+        }
+      } else if (warp == kReduceWarp) {
+        // ==================== dQ_part into the fp32 accumulator ==============
+        if (lane == 0 && n_iter > 0) {
+            tma_prefetch_map(&tm_dq);
+            for (int it = 0; it < n_iter; ++it) {
+                const int s = it & 1;
+                if (!wait_bar(smem_u32(&bars->dstage_full[s]), (it >> 1) & 1, abort, kErrBwdWait + 13))
+                    break;
+                const int h = head_of(it), qt = qtile_of(it);
+                for (int j = 0; j < D / 32; ++j) {
+                    const uint32_t slice = (j < D / 64 ? sQ + (uint32_t)(j * kSliceBytes)
+                                                       : sDO + (uint32_t)((j - D / 64) * kSliceBytes)) +
+                                           (uint32_t)(s * L::kTileBytes);
+                    tma_reduce_add_4d(&tm_dq, slice, 32 * j, h, qt * kBlockM, b);   // rows past Sq are clipped
+                }
+                bulk_commit_group();
+                bulk_wait_group_read0();                    // stage s may be refilled
+                mbar_arrive(smem_u32(&bars->q_empty[s]));
+            }
+            bulk_wait_group0();                             // the reductions have landed
         }
       }
     } else if (warp < kDqWarp0) {
@@ -390,28 +417,35 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t dp_t = tmem + lane_addr + L::kColDP;
         const float c = p.scale_log2;
         const bool key_ok = key < p.Skv;
-        // LSE2 / Delta of query row kr of iteration `it` (+inf / 0 past Sq)
-        auto stat_of = [&](int it, float& l2, float& dl) {
+        // LSE and Delta of query row kr of iteration `it` as loaded (0 past
+        // Sq), and LSE2 as stored (+inf past Sq): loaded a tile ahead and
+        // used only at the store, so the load latency stays off the tile
+        bool nv = false;
+        auto stat_load = [&](int it, float& lse, float& dl) {
             const int qrow = qtile_of(it) * kBlockM + kr;
             const int64_t at = ((int64_t)b * p.Hq + head_of(it)) * p.Sq + qrow;
-            l2 = qrow < p.Sq ? p.lse[at] * kLog2e : INFINITY;
-            dl = qrow < p.Sq ? p.delta[at] : 0.f;
+            nv = qrow < p.Sq;
+            lse = nv ? p.lse[at] : 0.f;
+            dl = nv ? p.delta[at] : 0.f;
+        };
+        auto stat_store = [&](float* buf, float lse, float dl) {
+            buf[kr] = nv ? lse * kLog2e : INFINITY;
+            buf[kBlockM + kr] = dl;
         };
         // the first warpgroup keeps the statistics buffers
         if (n_iter > 0 && sw == 0) {
-            float l2, dl;
-            stat_of(0, l2, dl);
-            stats[kr] = l2;
-            stats[kBlockM + kr] = dl;
+            float l0, d0;
+            stat_load(0, l0, d0);
+            stat_store(stats, l0, d0);
             mbar_arrive(smem_u32(&bars->stats_full[0]));
         }
         bool ok = true;
         for (int it = 0; ok && it < n_iter; ++it) {
             ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full), it & 1, abort, kErrBwdWait + 6));
-            // the next tile's LSE2 / Delta: loaded now, stored after this tile
+            // the next tile's LSE / Delta: loaded now, stored after this tile
             float nl2 = 0.f, ndl = 0.f;
             if (sw == 0 && it + 1 < n_iter)
-                stat_of(it + 1, nl2, ndl);
+                stat_load(it + 1, nl2, ndl);
             if (ok)
                 ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->stats_full[it & 1]), (it >> 1) & 1, abort,
                                                       kErrBwdWait + 9));
@@ -455,10 +489,6 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // packed over the warpgroup's own dP^T columns and into the
             // shared tile for dQ
             ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->dp_full), it & 1, abort, kErrBwdWait + 11));
-            // the dS^T tile doubles as the dQ staging buffer of the last tile
-            if (ok && it > 0)
-                ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->dstage_free), (it - 1) & 1, abort,
-                                                      kErrBwdWait + 12));
             if (!ok)
                 break;
             tc_fence_after_sync();
@@ -498,9 +528,7 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // readers (tile it - 1, both phases) finished before that tile's
             // ds_ready, which came before this tile's S was issued
             if (sw == 0 && it + 1 < n_iter) {
-                float* nb = stats + ((it + 1) & 1) * 2 * kBlockM;
-                nb[kr] = nl2;
-                nb[kBlockM + kr] = ndl;
+                stat_store(stats + ((it + 1) & 1) * 2 * kBlockM, nl2, ndl);
                 mbar_arrive(smem_u32(&bars->stats_full[(it + 1) & 1]));
             }
         }
@@ -547,7 +575,6 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t src = tmem + ((uint32_t)(quarter * 32) << 16) + L::kColDP;   // dQ_part
         bool ok = true;
         for (int it = 0; ok && it < n_iter; ++it) {
-            const int h = head_of(it), qt = qtile_of(it);
             ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->dq_full), it & 1, abort, kErrBwdWait + 8));
             if (!ok)
                 break;
@@ -560,46 +587,27 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld32_wait(src + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
             tc_fence_before_sync();
             mbar_arrive(smem_u32(&bars->dq_free));
-            // into the fp32 accumulator by TMA reductions: 32-column slices
-            // (128 rows x 128 bytes, 128-byte swizzle) staged in the dS^T
-            // tile, two slices per round
+            // staged for the reducer over Q / dO stage s (free: every MMA of
+            // the tile has completed): 32-column slices of 128 rows x 128
+            // bytes with the 128-byte swizzle, slices 0 .. D/64-1 over Q and
+            // the rest over dO
+            const int s = it & 1;
 #pragma unroll
-            for (int hh = 0; hh < D / 64; ++hh) {
+            for (int j = 0; j < D / 32; ++j) {
+                const uint32_t slice = (j < D / 64 ? sQ + (uint32_t)(j * kSliceBytes)
+                                                   : sDO + (uint32_t)((j - D / 64) * kSliceBytes)) +
+                                       (uint32_t)(s * L::kTileBytes);
+                const uint32_t row = slice + (uint32_t)(qr * 128);
 #pragma unroll
-                for (int box = 0; box < 2; ++box) {
-                    const uint32_t row = sDS + box * L::kDSChunkBytes + qr * 128;
-                    const int c0 = 64 * hh + 32 * box;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        st_shared_v4(row + (uint32_t)((u ^ (qr & 7)) << 4), r[c0 + 4 * u], r[c0 + 4 * u + 1],
-                                     r[c0 + 4 * u + 2], r[c0 + 4 * u + 3]);
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(smem_u32(&bars->dstage_full));
-                const uint32_t round = (uint32_t)(it * (D / 64) + hh);
-                if (threadIdx.x == kDqWarp0 * 32) {
-                    if (wait_bar(smem_u32(&bars->dstage_full), round & 1, abort, kErrBwdWait + 13)) {
-                        for (int box = 0; box < 2; ++box)
-                            tma_reduce_add_4d(&tm_dq, sDS + box * L::kDSChunkBytes, 64 * hh + 32 * box, h,
-                                              qt * kBlockM, b);
-                        bulk_commit_group();
-                        bulk_wait_group_read0();            // the staging buffer may be overwritten
-                    }
-                    mbar_arrive(smem_u32(&bars->dstage_read));
-                }
-                __syncwarp();
-                ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->dstage_read), round & 1, abort,
-                                                      kErrBwdWait + 14));
-                if (!ok)
-                    break;
+                for (int u = 0; u < 8; ++u)
+                    st_shared_v4(row + (uint32_t)((u ^ (qr & 7)) << 4), r[32 * j + 4 * u], r[32 * j + 4 * u + 1],
+                                 r[32 * j + 4 * u + 2], r[32 * j + 4 * u + 3]);
             }
-            if (ok && threadIdx.x == kDqWarp0 * 32)
-                mbar_arrive(smem_u32(&bars->dstage_free));
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&bars->dstage_full[s]));
         }
     }
 
-    if (threadIdx.x == kDqWarp0 * 32)
-        bulk_wait_group0();                                 // the reductions have landed
     tc_fence_before_sync();
     __syncthreads();
     if (warp == kMmaWarp) {
