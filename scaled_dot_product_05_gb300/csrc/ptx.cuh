@@ -45,6 +45,22 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// True if the phase with the given parity has completed, without waiting.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // True once the phase with the given parity has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
@@ -118,6 +134,12 @@ __device__ __forceinline__ void bulk_commit_group()
 __device__ __forceinline__ void bulk_wait_group_read0()
 {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// ... all but the most recent bulk group have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_group_read1()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 __device__ __forceinline__ void bulk_wait_group0()

@@ -51,6 +51,7 @@ constexpr int kThreads = 512;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kReduceWarp = 2;
+constexpr int kStatsWarp = 3;
 constexpr int kSoftmaxWarp0 = 4;     // warps 4..11: two warpgroups, 64 queries each
 constexpr int kDqWarp0 = 12;         // warps 12..15
 // Register split: launched at 128 per thread (512 x 128 = 65536); warps 0..3
@@ -82,8 +83,10 @@ struct Params {
 
 struct BwdBarriers {
     uint64_t kv_full;
-    uint64_t q_full[2];
-    uint64_t q_empty[2];
+    uint64_t q_full[2];              // Q tile of stage s loaded
+    uint64_t q_empty[2];             // Q tile of stage s free (its dQ slices reduced)
+    uint64_t do_full[2];             // dO tile of stage s loaded
+    uint64_t do_empty[2];            // dO tile of stage s free
     uint64_t s_full;                 // S^T in TMEM
     uint64_t dp_full;                // dP^T in TMEM
     uint64_t p_ready;                // P^T packed in TMEM (both softmax warpgroups)
@@ -91,8 +94,8 @@ struct BwdBarriers {
     uint64_t dq_full;
     uint64_t dq_free;
     uint64_t dkv_full;
-    uint64_t stats_full[2];          // LSE2 / Delta buffer written (count 128)
-    uint64_t dstage_full[2];         // dQ_part staged over Q / dO stage s (count 128)
+    uint64_t stats_full[2];          // LSE2 / Delta buffer written (count 32)
+    uint64_t dstage_full[2][4];      // dQ_part slice j staged over Q / dO stage s (count 128)
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -125,6 +128,7 @@ struct BwdLayout {
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
     static_assert(sizeof(BwdBarriers) <= 256, "barrier block");
+    static_assert(D / 32 <= 4, "staging barriers: one per 32-column slice");
     static_assert(kColDK + D <= 512, "TMEM columns");
 };
 
@@ -231,6 +235,8 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&bars->q_full[s]), 1);
             mbar_init(smem_u32(&bars->q_empty[s]), 1);
+            mbar_init(smem_u32(&bars->do_full[s]), 1);
+            mbar_init(smem_u32(&bars->do_empty[s]), 1);
         }
         mbar_init(smem_u32(&bars->s_full), 1);
         mbar_init(smem_u32(&bars->dp_full), 1);
@@ -239,10 +245,11 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(smem_u32(&bars->dq_full), 1);
         mbar_init(smem_u32(&bars->dq_free), 128);
         mbar_init(smem_u32(&bars->dkv_full), 1);
-        mbar_init(smem_u32(&bars->stats_full[0]), 128);
-        mbar_init(smem_u32(&bars->stats_full[1]), 128);
-        mbar_init(smem_u32(&bars->dstage_full[0]), 128);
-        mbar_init(smem_u32(&bars->dstage_full[1]), 128);
+        mbar_init(smem_u32(&bars->stats_full[0]), 32);
+        mbar_init(smem_u32(&bars->stats_full[1]), 32);
+        for (int s = 0; s < 2; ++s)
+            for (int j = 0; j < 4; ++j)
+                mbar_init(smem_u32(&bars->dstage_full[s][j]), 128);
         mbar_init(smem_u32(&bars->drain), 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -276,24 +283,35 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             int issued = 0;
             for (int it = 0; it < n_iter; ++it) {
                 const int s = it & 1;
+                // Q and dO of a stage are freed separately (the reducer reads
+                // the dQ slices staged over Q first): Q, which S^T needs
+                // first, is refilled as soon as it is free
+                const int h = head_of(it), qt = qtile_of(it);
                 if (it >= 2 &&
                     !wait_bar(smem_u32(&bars->q_empty[s]), ((it >> 1) & 1) ^ 1, abort, kErrBwdWait + 1))
                     break;
-                const int h = head_of(it), qt = qtile_of(it);
-                mbar_arrive_expect_tx(smem_u32(&bars->q_full[s]), 2 * L::kTileBytes);
-                for (int c = 0; c < L::kChunks; ++c) {
+                mbar_arrive_expect_tx(smem_u32(&bars->q_full[s]), L::kTileBytes);
+                for (int c = 0; c < L::kChunks; ++c)
                     tma_load_4d(sQ + s * L::kTileBytes + c * L::kChunkBytes, &tm_q, smem_u32(&bars->q_full[s]),
                                 c * kCe, h, qt * kBlockM, b);
-                    tma_load_4d(sDO + s * L::kTileBytes + c * L::kChunkBytes, &tm_do, smem_u32(&bars->q_full[s]),
+                ++issued;
+                if (it >= 2 &&
+                    !wait_bar(smem_u32(&bars->do_empty[s]), ((it >> 1) & 1) ^ 1, abort, kErrBwdWait + 12))
+                    break;
+                mbar_arrive_expect_tx(smem_u32(&bars->do_full[s]), L::kTileBytes);
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_4d(sDO + s * L::kTileBytes + c * L::kChunkBytes, &tm_do, smem_u32(&bars->do_full[s]),
                                 c * kCe, h, qt * kBlockM, b);
-                }
                 ++issued;
             }
             if (*abort) {
                 // never leave the CTA with copies in flight
                 drain_wait(smem_u32(&bars->kv_full), 0);
-                for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
-                    drain_wait(smem_u32(&bars->q_full[it & 1]), (it >> 1) & 1);
+                // issued counts the loads in order (Q of a tile, then its dO)
+                for (int k = (issued > 4 ? issued - 4 : 0); k < issued; ++k) {
+                    const int it = k >> 1;
+                    drain_wait(smem_u32(&((k & 1) ? bars->do_full : bars->q_full)[it & 1]), (it >> 1) & 1);
+                }
             }
         }
     } else if (warp == kMmaWarp) {
@@ -314,28 +332,35 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t ds_lo = (sDS >> 4) | ((uint32_t)(L::kDSChunkBytes >> 4) << 16);
             const uint32_t s_t = tmem + L::kColS, dp_t = tmem + L::kColDP;
             const uint32_t dv_t = tmem + L::kColDV, dk_t = tmem + L::kColDK;
-            bool ok = wait_bar(smem_u32(&bars->kv_full), 0, abort, kErrBwdWait + 2);
-            for (int it = 0; ok && it < n_iter; ++it) {
+            // S^T = K Q^T (keys x queries, K = D) of tile `it` into cols 0..127
+            auto issue_s = [&](int it) -> bool {
                 const int s = it & 1;
-                ok = wait_bar(smem_u32(&bars->q_full[s]), (it >> 1) & 1, abort, kErrBwdWait + 3);
-                if (!ok)
-                    break;
+                if (!wait_bar(smem_u32(&bars->q_full[s]), (it >> 1) & 1, abort, kErrBwdWait + 3))
+                    return false;
                 tc_fence_after_sync();
                 const uint32_t q_lo = ((sQ + s * L::kTileBytes) >> 4) | kmaj;
-                const uint32_t q_mn = ((sQ + s * L::kTileBytes) >> 4) | mnmaj;
-                const uint32_t do_lo = ((sDO + s * L::kTileBytes) >> 4) | kmaj;
-                const uint32_t do_mn = ((sDO + s * L::kTileBytes) >> 4) | mnmaj;
-                // S^T = K Q^T (keys x queries, K = D) into cols 0..127: the last
-                // tile's P^T there was read by its dV MMA, issued before this one
 #pragma unroll
                 for (int kk = 0; kk < L::kSteps; ++kk) {
                     const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
                     mma_f16_ss(s_t, desc_join(hi, k_lo + off), desc_join(hi, q_lo + off), id_s, kk > 0);
                 }
                 mma_commit(smem_u32(&bars->s_full));
+                return true;
+            };
+            bool ok = wait_bar(smem_u32(&bars->kv_full), 0, abort, kErrBwdWait + 2);
+            if (ok)
+                ok = issue_s(0);
+            for (int it = 0; ok && it < n_iter; ++it) {
+                const int s = it & 1;
+                bool s_next = it + 1 >= n_iter;             // the next tile's S^T issued
+                const uint32_t q_mn = ((sQ + s * L::kTileBytes) >> 4) | mnmaj;
+                const uint32_t do_lo = ((sDO + s * L::kTileBytes) >> 4) | kmaj;
+                const uint32_t do_mn = ((sDO + s * L::kTileBytes) >> 4) | mnmaj;
                 // dP^T = V dO^T into cols 128..255, once the dQ warps have read the
                 // last tile's dQ_part out of them
                 if (it > 0 && !(ok = wait_bar(smem_u32(&bars->dq_free), (it - 1) & 1, abort, kErrBwdWait + 4)))
+                    break;
+                if (!(ok = wait_bar(smem_u32(&bars->do_full[s]), (it >> 1) & 1, abort, kErrBwdWait + 14)))
                     break;
                 tc_fence_after_sync();
 #pragma unroll
@@ -356,6 +381,15 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
                     const uint32_t col = (kk < 4) ? 8 * kk : 32 + 8 * kk;
                     mma_f16_ts(dv_t, s_t + col, desc_join(hi, do_mn + off), id_o, acc);
+                }
+                // the next tile's S^T right after this dV MMA (the last reader of
+                // cols 0..127) if its Q has landed: it runs while the softmax
+                // forms dS^T, so the next P^T can start when this dS^T is done.
+                // Otherwise after the dQ MMA, not to hold up dK and dQ.
+                if (!s_next && mbar_test_wait(smem_u32(&bars->q_full[(it + 1) & 1]), ((it + 1) >> 1) & 1)) {
+                    if (!(ok = issue_s(it + 1)))
+                        break;
+                    s_next = true;
                 }
                 // dK += dS^T Q, dS^T from TMEM like P^T; Q MN-major
                 if (!(ok = wait_bar(smem_u32(&bars->ds_ready), it & 1, abort, kErrBwdWait + 10)))
@@ -378,6 +412,8 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mma_f16_ss(dp_t, desc_join(hi_ds, ds_lo + off_a), desc_join(hi, k_mn + off_b), id_q, kk > 0);
                 }
                 mma_commit(smem_u32(&bars->dq_full));       // also frees Q / dO stage s for dQ staging
+                if (!s_next && !(ok = issue_s(it + 1)))
+                    break;
             }
             mma_commit(smem_u32(&bars->dkv_full));
             mma_commit(smem_u32(&bars->drain));
@@ -389,20 +425,55 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tma_prefetch_map(&tm_dq);
             for (int it = 0; it < n_iter; ++it) {
                 const int s = it & 1;
-                if (!wait_bar(smem_u32(&bars->dstage_full[s]), (it >> 1) & 1, abort, kErrBwdWait + 13))
-                    break;
                 const int h = head_of(it), qt = qtile_of(it);
-                for (int j = 0; j < D / 32; ++j) {
-                    const uint32_t slice = (j < D / 64 ? sQ + (uint32_t)(j * kSliceBytes)
-                                                       : sDO + (uint32_t)((j - D / 64) * kSliceBytes)) +
-                                           (uint32_t)(s * L::kTileBytes);
-                    tma_reduce_add_4d(&tm_dq, slice, 32 * j, h, qt * kBlockM, b);   // rows past Sq are clipped
+                // each slice as soon as it is staged, those over Q first, then
+                // those over dO: two bulk groups
+                bool staged = true;
+                for (int half = 0; staged && half < 2; ++half) {
+                    for (int j = half * (D / 64); j < (half + 1) * (D / 64); ++j) {
+                        if (!(staged = wait_bar(smem_u32(&bars->dstage_full[s][j]), (it >> 1) & 1, abort,
+                                                kErrBwdWait + 13)))
+                            break;
+                        const uint32_t slice = (half == 0 ? sQ + (uint32_t)(j * kSliceBytes)
+                                                          : sDO + (uint32_t)((j - D / 64) * kSliceBytes)) +
+                                               (uint32_t)(s * L::kTileBytes);
+                        tma_reduce_add_4d(&tm_dq, slice, 32 * j, h, qt * kBlockM, b);   // rows past Sq are clipped
+                    }
+                    bulk_commit_group();
                 }
-                bulk_commit_group();
-                bulk_wait_group_read0();                    // stage s may be refilled
+                if (!staged)
+                    break;
+                bulk_wait_group_read1();                    // Q of stage s may be refilled
                 mbar_arrive(smem_u32(&bars->q_empty[s]));
+                bulk_wait_group_read0();                    // and its dO
+                mbar_arrive(smem_u32(&bars->do_empty[s]));
             }
             bulk_wait_group0();                             // the reductions have landed
+        }
+      } else if (warp == kStatsWarp) {
+        // ====================== LSE2 / Delta of each tile =====================
+        // Four query rows per lane into buffer it & 1: LSE2 = LSE log2(e)
+        // (+inf past Sq: no weight) and Delta.  The buffer of tile it + 1 is
+        // written once p_ready of tile it shows both softmax warpgroups done
+        // with tile it - 1, its last readers; the wait is one tile ahead of
+        // its use, and p_ready of tile it + 1 cannot come before this write.
+        for (int it = 0; it < n_iter; ++it) {
+            if (it > 0 &&
+                !__all_sync(0xffffffffu, wait_bar(smem_u32(&bars->p_ready), (it - 1) & 1, abort, kErrBwdWait + 16)))
+                break;
+            const int qr0 = qtile_of(it) * kBlockM + 4 * lane;
+            const int64_t row = ((int64_t)b * p.Hq + head_of(it)) * p.Sq;
+            float l2[4], dl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const bool v = qr0 + e < p.Sq;
+                l2[e] = v ? p.lse[row + qr0 + e] * kLog2e : INFINITY;
+                dl[e] = v ? p.delta[row + qr0 + e] : 0.f;
+            }
+            float4* buf = reinterpret_cast<float4*>(stats + (it & 1) * 2 * kBlockM);
+            buf[lane] = make_float4(l2[0], l2[1], l2[2], l2[3]);
+            buf[kBlockM / 4 + lane] = make_float4(dl[0], dl[1], dl[2], dl[3]);
+            mbar_arrive(smem_u32(&bars->stats_full[it & 1]));
         }
       }
     } else if (warp < kDqWarp0) {
@@ -417,35 +488,9 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t dp_t = tmem + lane_addr + L::kColDP;
         const float c = p.scale_log2;
         const bool key_ok = key < p.Skv;
-        // LSE and Delta of query row kr of iteration `it` as loaded (0 past
-        // Sq), and LSE2 as stored (+inf past Sq): loaded a tile ahead and
-        // used only at the store, so the load latency stays off the tile
-        bool nv = false;
-        auto stat_load = [&](int it, float& lse, float& dl) {
-            const int qrow = qtile_of(it) * kBlockM + kr;
-            const int64_t at = ((int64_t)b * p.Hq + head_of(it)) * p.Sq + qrow;
-            nv = qrow < p.Sq;
-            lse = nv ? p.lse[at] : 0.f;
-            dl = nv ? p.delta[at] : 0.f;
-        };
-        auto stat_store = [&](float* buf, float lse, float dl) {
-            buf[kr] = nv ? lse * kLog2e : INFINITY;
-            buf[kBlockM + kr] = dl;
-        };
-        // the first warpgroup keeps the statistics buffers
-        if (n_iter > 0 && sw == 0) {
-            float l0, d0;
-            stat_load(0, l0, d0);
-            stat_store(stats, l0, d0);
-            mbar_arrive(smem_u32(&bars->stats_full[0]));
-        }
         bool ok = true;
         for (int it = 0; ok && it < n_iter; ++it) {
             ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full), it & 1, abort, kErrBwdWait + 6));
-            // the next tile's LSE / Delta: loaded now, stored after this tile
-            float nl2 = 0.f, ndl = 0.f;
-            if (sw == 0 && it + 1 < n_iter)
-                stat_load(it + 1, nl2, ndl);
             if (ok)
                 ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->stats_full[it & 1]), (it >> 1) & 1, abort,
                                                       kErrBwdWait + 9));
@@ -524,13 +569,6 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(smem_u32(&bars->ds_ready));
-            // the next tile's statistics into the other buffer: its last
-            // readers (tile it - 1, both phases) finished before that tile's
-            // ds_ready, which came before this tile's S was issued
-            if (sw == 0 && it + 1 < n_iter) {
-                stat_store(stats + ((it + 1) & 1) * 2 * kBlockM, nl2, ndl);
-                mbar_arrive(smem_u32(&bars->stats_full[(it + 1) & 1]));
-            }
         }
         // ---- dK, dV of this key (dK carries the scale already, through dS) ----
         // The wait and the TMEM loads are warp-wide (every lane takes part);
@@ -602,9 +640,9 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int u = 0; u < 8; ++u)
                     st_shared_v4(row + (uint32_t)((u ^ (qr & 7)) << 4), r[32 * j + 4 * u], r[32 * j + 4 * u + 1],
                                  r[32 * j + 4 * u + 2], r[32 * j + 4 * u + 3]);
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&bars->dstage_full[s][j]));   // the reducer may start on it
             }
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bars->dstage_full[s]));
         }
     }
 
