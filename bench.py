@@ -57,6 +57,9 @@ DECODE_WORKLOADS = {
 # backward pass (gradients of sum(dO * O)): name -> (B, Hq, Hkv, S, D, causal)
 BWD_WORKLOADS = {
     "bwd-gqa-causal-4096": (2, 32, 8, 4096, 128, True),
+    "bwd-mqa-causal-4096": (8, 32, 1, 4096, 128, True),
+    "bwd-mqa-full-16384": (2, 32, 1, 16384, 128, False),
+    "bwd-mha-causal-1024": (4, 16, 16, 1024, 64, True),
 }
 DEFAULT_WORKLOAD = "gqa-causal-4096"
 
@@ -115,12 +118,14 @@ def n_rotating_sets(name):
     return int(min(4096, max(2, -(-2 * L2_BYTES // step_bytes(name)))))
 
 
-def kernel_source_hash():
-    """Hash of the kernels' own sources (device code): a stored DRAM traffic
-    figure is used only while they are unchanged."""
+def kernel_source_hash(name=None):
+    """Hash of the timed kernel's own sources (device code) for workload
+    `name`: a stored DRAM traffic figure is used only while they are
+    unchanged.  The backward kernel also includes the forward's header."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "scaled_dot_product_05_gb300", "csrc")
-    for f in ("sdpa_kernel.cuh", "ptx.cuh"):
+    files = ("sdpa_bwd.cuh", "sdpa_kernel.cuh", "ptx.cuh") if name in BWD_WORKLOADS else ("sdpa_kernel.cuh", "ptx.cuh")
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -144,7 +149,7 @@ def stored_traffic(name):
     with open(path) as f:
         t = json.load(f)
     e = t.get(name)
-    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+    if not e or e.get("kernel_source_hash") != kernel_source_hash(name):
         return None
     return e.get("dram_bytes_per_launch")
 

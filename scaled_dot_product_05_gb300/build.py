@@ -10,7 +10,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libsdpa_gb300.so")
 SOURCES = ["sdpa_api.cu"]
-HEADERS = ["sdpa_kernel.cuh", "ptx.cuh"]
+HEADERS = ["sdpa_kernel.cuh", "sdpa_bwd.cuh", "sdpa_bwd_prep.cuh", "ptx.cuh"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-shared"]
 

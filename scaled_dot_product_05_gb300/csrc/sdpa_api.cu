@@ -15,6 +15,7 @@
 #include "../../include/sdpa.h"
 #include "sdpa_kernel.cuh"
 #include "sdpa_bwd.cuh"
+#include "sdpa_bwd_prep.cuh"
 
 namespace {
 
@@ -568,8 +569,10 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(float), stream);
     if (e != cudaSuccess)
         return e;
-    sdpa::bwd::bwd_delta_kernel<D, kBF16><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
-        O, dO, const_cast<float*>(p.delta), p.B, p.Hq, p.Sq);
+    constexpr int kRows = sdpa::bwd::delta_rows_per_block<D>();
+    sdpa::bwd::bwd_delta_kernel<D, kBF16>
+        <<<static_cast<unsigned>((rows + kRows - 1) / kRows), sdpa::bwd::kDeltaThreads, 0, stream>>>(
+            O, dO, const_cast<float*>(p.delta), p.B, p.Hq, p.Sq);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
     const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.n_kt);

@@ -33,7 +33,8 @@
 //                  reads them precedes the dQ MMA; 128 x D fp32 is exactly
 //                  their size), for the reducer (every key tile of a query
 //                  row contributes to its dQ)
-// A preprocessing kernel forms Delta, a final one converts the fp32 dQ.
+// A preprocessing kernel forms Delta, a final one converts the fp32 dQ
+// (both in sdpa_bwd_prep.cuh).
 #pragma once
 
 #include <cstdint>
@@ -139,54 +140,6 @@ struct BwdLayout {
 __device__ __forceinline__ int bwd_qt0(const Params& p, int kt)
 {
     return p.causal ? kt : 0;
-}
-
-// Delta_i = dO_i . O_i (fp32), one warp per row (b, hq, i) of the
-// [B][Hq][Sq] layout; dO and O are [B][Sq][Hq][D] 16-bit.
-template <int D, bool kBF16>
-__global__ void __launch_bounds__(128) bwd_delta_kernel(const void* O, const void* dO, float* delta, int B, int Hq,
-                                                       int Sq)
-{
-    const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= (int64_t)B * Hq * Sq)
-        return;
-    const int i = (int)(row % Sq);
-    const int64_t bh = row / Sq;
-    const int hq = (int)(bh % Hq);
-    const int b = (int)(bh / Hq);
-    const int64_t off = (((int64_t)b * Sq + i) * Hq + hq) * D;
-    float acc = 0.f;
-    for (int d = lane; d < D; d += 32) {
-        float o, g;
-        if constexpr (kBF16) {
-            o = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(O)[off + d]);
-            g = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(dO)[off + d]);
-        } else {
-            o = __half2float(reinterpret_cast<const __half*>(O)[off + d]);
-            g = __half2float(reinterpret_cast<const __half*>(dO)[off + d]);
-        }
-        acc += o * g;
-    }
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1)
-        acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0)
-        delta[row] = acc;
-}
-
-// dQ (16-bit, [B][Sq][Hq][D]) from the fp32 accumulator, 4 elements a thread.
-template <bool kBF16>
-__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* acc, void* dQ, int64_t n)
-{
-    const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
-    if (i >= n)
-        return;
-    const float4 v = *reinterpret_cast<const float4*>(acc + i);
-    uint2 out;
-    out.x = pack2<kBF16>(v.x, v.y);
-    out.y = pack2<kBF16>(v.z, v.w);
-    *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(dQ) + i) = out;
 }
 
 template <int D, int KIND>
