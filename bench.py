@@ -54,12 +54,14 @@ DECODE_WORKLOADS = {
     "decode-gqa-b8-32k": (8, 32, 8, 1, 32768, 128),
     "decode-gqa-b32-8k": (32, 32, 8, 4, 8192, 128),
 }
-# backward pass (gradients of sum(dO * O)): name -> (B, Hq, Hkv, S, D, causal)
+# backward pass (gradients of sum(dO * O)): name -> (B, Hq, Hkv, S, D, causal[, dtype]);
+# "e4m3": the FP8 pass (E4M3 Q, K, V, E5M2 dO) on the FP8 forward's shape
 BWD_WORKLOADS = {
     "bwd-gqa-causal-4096": (2, 32, 8, 4096, 128, True),
     "bwd-mqa-causal-4096": (8, 32, 1, 4096, 128, True),
     "bwd-mqa-full-16384": (2, 32, 1, 16384, 128, False),
     "bwd-mha-causal-1024": (4, 16, 16, 1024, 64, True),
+    "bwd-fp8-causal-8192": (2, 16, 16, 8192, 128, True, "e4m3"),
 }
 DEFAULT_WORKLOAD = "gqa-causal-4096"
 
@@ -74,8 +76,8 @@ class Spec(tuple):
 
 def spec(name):
     if name in BWD_WORKLOADS:
-        B, Hq, Hkv, S, D, causal = BWD_WORKLOADS[name]
-        return Spec((B, Hq, Hkv, S, S, D, causal, "bf16", False))
+        B, Hq, Hkv, S, D, causal, *dt = BWD_WORKLOADS[name]
+        return Spec((B, Hq, Hkv, S, S, D, causal, dt[0] if dt else "bf16", False))
     if name in DECODE_WORKLOADS:
         B, Hq, Hkv, Sq, Skv, D = DECODE_WORKLOADS[name]
         return Spec((B, Hq, Hkv, Sq, Skv, D, False, "bf16", True))
@@ -107,7 +109,8 @@ def step_bytes(name):
     Q, K, V, O, dO and the LSE read, dQ, dK, dV written)."""
     w = spec(name)
     if name in BWD_WORKLOADS:
-        return 2 * w.B * w.D * (3 * w.Sq * w.Hq + 4 * w.Skv * w.Hkv) + 4 * w.B * w.Hq * w.Sq
+        e = 1 if w.dtype == "e4m3" else 2        # Q, K, V, dO; O and the gradients are 16-bit
+        return w.B * w.D * (w.Sq * w.Hq * (2 * e + 4) + w.Skv * w.Hkv * (2 * e + 4)) + 4 * w.B * w.Hq * w.Sq
     e_in = 1 if w.dtype == "e4m3" else 2
     return w.B * w.D * (w.Sq * w.Hq * e_in + 2 * w.Skv * w.Hkv * e_in + w.Sq * w.Hq * 2)
 
@@ -124,7 +127,11 @@ def kernel_source_hash(name=None):
     unchanged.  The backward kernel also includes the forward's header."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "scaled_dot_product_05_gb300", "csrc")
-    files = ("sdpa_bwd.cuh", "sdpa_kernel.cuh", "ptx.cuh") if name in BWD_WORKLOADS else ("sdpa_kernel.cuh", "ptx.cuh")
+    if name in BWD_WORKLOADS:
+        files = (("sdpa_bwd_fp8.cuh",) if spec(name).dtype == "e4m3" else ()) + ("sdpa_bwd.cuh", "sdpa_kernel.cuh",
+                                                                                 "ptx.cuh")
+    else:
+        files = ("sdpa_kernel.cuh", "ptx.cuh")
     for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
@@ -572,34 +579,58 @@ def run_gpu_bwd(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
 
-    from scaled_dot_product_05_gb300 import bwd_workspace_bytes, sdpa_bwd, sdpa_device_error, sdpa_fwd_ex
-    from sdpa_inputs import make_qkv
+    from scaled_dot_product_05_gb300 import (bwd_fp8_workspace_bytes, bwd_workspace_bytes, sdpa_bwd, sdpa_bwd_fp8,
+                                              sdpa_device_error, sdpa_fwd_ex, sdpa_fwd_fp8_ex)
+    from sdpa_inputs import E5M2_MAX, make_grad, make_qkv
 
     name = args.workload
     w = spec(name)
     B, Hq, Hkv, S, D, causal = w.B, w.Hq, w.Hkv, w.Sq, w.D, w.causal
+    fp8 = w.dtype == "e4m3"
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     n_sets = n_rotating_sets(name)
     sets = []
     host = None
+    descales = []                    # FP8: (dq, dk, dv, ddo, scale_ds) per set
     for i in range(n_sets):
-        x = make_qkv(100 + 17 * rank + i, B, Hq, Hkv, S, S, D, "bf16")
-        do = make_qkv(200 + 17 * rank + i, B, Hq, Hkv, S, S, D, "bf16").q
+        if fp8:
+            x = make_qkv(100 + 17 * rank + i, B, Hq, Hkv, S, S, D, "e4m3")
+            do, ddo = make_grad(200 + 17 * rank + i, (B, S, Hq, D), "e5m2")
+        else:
+            x = make_qkv(100 + 17 * rank + i, B, Hq, Hkv, S, S, D, "bf16")
+            do = make_grad(200 + 17 * rank + i, (B, S, Hq, D), "bf16")
         q, k, v, g = (t.to(dev) for t in (x.q, x.k, x.v, do))
-        o = torch.empty_like(q)
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
         lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
-        sdpa_fwd_ex(q, k, v, o, lse, causal=causal)
-        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        if fp8:
+            sdpa_fwd_fp8_ex(q, k, v, o, lse, descale_q=x.descales[0], descale_k=x.descales[1],
+                            descale_v=x.descales[2], causal=causal)
+            grads = tuple(torch.empty(t.shape, dtype=torch.bfloat16, device=dev) for t in (q, k, v))
+        else:
+            sdpa_fwd_ex(q, k, v, o, lse, causal=causal)
+            grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
         sets.append((q, k, v, o, g, lse, grads))
+        if fp8:
+            # the recipe's delayed scale of dS: amax of a first call
+            amax = torch.zeros(1, dtype=torch.float32, device=dev)
+            sdpa_bwd_fp8(q, k, v, o, g, lse, *grads, descale_q=x.descales[0], descale_k=x.descales[1],
+                         descale_v=x.descales[2], descale_do=ddo, scale_ds=1.0, amax_ds=amax, causal=causal)
+            descales.append((*x.descales, ddo, E5M2_MAX / float(amax.item())))
         if i == 0:
             host = tuple(t.cpu().pin_memory() for t in (q, k, v, o, g, lse))
-    ws = torch.empty(bwd_workspace_bytes(B, Hq, S, D), dtype=torch.uint8, device=dev)
+    ws_bytes = bwd_fp8_workspace_bytes(B, Hq, S, D) if fp8 else bwd_workspace_bytes(B, Hq, S, D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
     def launch(i, st=None):
         q, k, v, o, g, lse, (dq, dk, dv) = sets[i % n_sets]
-        sdpa_bwd(q, k, v, o, g, lse, dq, dk, dv, causal=causal, workspace=ws, stream=st or stream)
+        if fp8:
+            a, b_, c, d, sds = descales[i % n_sets]
+            sdpa_bwd_fp8(q, k, v, o, g, lse, dq, dk, dv, descale_q=a, descale_k=b_, descale_v=c, descale_do=d,
+                         scale_ds=sds, causal=causal, workspace=ws, stream=st or stream)
+        else:
+            sdpa_bwd(q, k, v, o, g, lse, dq, dk, dv, causal=causal, workspace=ws, stream=st or stream)
 
     def barrier():
         if world > 1:
@@ -661,16 +692,21 @@ def run_gpu_bwd(args, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     avg_kernel_ms = statistics.mean(kern_ms)
     achieved = flops / (avg_kernel_ms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"]
+    # FP8: twice the measured bf16 peak (the nominal dense FP8 / bf16 ratio)
+    peak = peaks["bf16_tflops"] * (2 if fp8 else 1)
+    peak_note = f"2 x bf16 burst ({peak_src}), the nominal FP8 / bf16 ratio" if fp8 else f"bf16 burst ({peak_src})"
     line = {
         "metric": METRIC, "value": whole_job_tflops(flops, world, ms_per_step), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), inputs resident in HBM)",
-        "config": {"workload": "backward pass, " + describe(name), "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": S, "Skv": S,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e5m2 (fp32 accumulate)" if fp8 else "bf16",
+        "data": "synthetic (seeded N(0,1), inputs resident in HBM)",
+        "config": {"workload": "backward pass, " + describe(name) + (" (E5M2 dO)" if fp8 else ""), "B": B, "Hq": Hq,
+                   "Hkv": Hkv, "Sq": S, "Skv": S,
                    "D": D, "causal": causal, "flops_per_step": flops, "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2 ({n_sets} rotating input sets of {step_bytes(name) / 1e6:.1f} MB)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": None, "peak_source": f"bf16 burst ({peak_src})", "kernel": "sdpa_bwd_kernel (+ Delta, "
+                     "traffic": stored_traffic(name), "peak_source": peak_note,
+                     "kernel": ("sdpa_bwd_fp8_kernel" if fp8 else "sdpa_bwd_kernel") + " (+ Delta, "
                      "dQ conversion; launch duration of the whole call)",
                      "algorithmic_bytes_per_launch": step_bytes(name)},
         "e2e": {"value": whole_job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,

@@ -221,6 +221,40 @@ sdpa_status_t sdpa_bwd(const void *Q, const void *K, const void *V, const void *
 size_t sdpa_bwd_workspace_bytes(int B, int Hq, int Sq, int D);
 
 /*
+ * FP8 backward pass (section 10 of the codelab, "FP8": E4M3 tensors in the
+ * forward pass, E5M2 for the backward pass), contiguous BSHD, D 64 or 128:
+ * the gradients of sum(dO * O) for O = sdpa_fwd_fp8(Q, K, V), every GEMM on
+ * the FP8 tensor cores with fp32 accumulation.
+ *   Q8, K8, V8  E4M3 codes (one byte each) of the forward's inputs, value =
+ *               code * descale_q / descale_k / descale_v.
+ *   O           the forward's bf16 output; LSE its log-sum-exp (fp32
+ *               [B][Hq][Sq], from sdpa_fwd_fp8_ex).
+ *   dO8         E5M2 codes of the upstream gradient, value = code * descale_do.
+ *   dQ, dK, dV  bf16, written, shaped like Q and K.
+ *   scale_ds    per-tensor scale of dS = P * (dP - Delta) before its E5M2
+ *               rounding (dS8 = e5m2(dS * scale_ds), saturating at 57344):
+ *               the delayed scale of the recipe, e.g. 57344 / amax of an
+ *               earlier step.  P is rounded to E4M3 as e4m3(448 P), P <= 1.
+ *   amax_ds     device float, written: max |dS| of this call (before
+ *               scaling), for the next call's scale_ds; NULL: not reported.
+ *   workspace   device scratch of at least sdpa_bwd_fp8_workspace_bytes(B,
+ *               Hq, Sq, D) bytes, 16-byte aligned, needing no
+ *               initialisation, not used by a concurrent call.
+ * Descales and scale_ds must be finite and > 0 (else SDPA_ERR_SCALE).
+ * Written buffers must not overlap one another or any input.  Other
+ * arguments and statuses as for sdpa_bwd.
+ */
+sdpa_status_t sdpa_bwd_fp8(const void *Q8, const void *K8, const void *V8, const void *O, const void *dO8,
+                           const float *LSE, void *dQ, void *dK, void *dV,
+                           int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                           float scale, int causal, float descale_q, float descale_k, float descale_v,
+                           float descale_do, float scale_ds, float *amax_ds,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes sdpa_bwd_fp8 needs (0 for invalid sizes). */
+size_t sdpa_bwd_fp8_workspace_bytes(int B, int Hq, int Sq, int D);
+
+/*
  * Workspace bytes sdpa_fwd_decode needs for this shape on the current device
  * (0: no split, or invalid sizes).  Initialises the library on the current
  * device on first use.
@@ -236,13 +270,14 @@ int sdpa_last_cuda_error(void);
 /*
  * Reads and clears the device error word of the current device (0 = none;
  * 0x1xx / 0x2xx / 0x3xx = a bounded wait of the producer / MMA issuer /
- * softmax gave up).  Synchronises the device.  Returns SDPA_OK or
+ * softmax gave up; 0x4xx / 0x5xx = a bounded wait of the 16-bit / FP8
+ * backward pass gave up).  Synchronises the device.  Returns SDPA_OK or
  * SDPA_ERR_CUDA; `code` (host pointer) receives the word.
  */
 sdpa_status_t sdpa_device_error(unsigned int *code);
 
 /* Version of this ABI (bumped on any change; 2 added the *_ex entry points, 3 the decode pass,
- * 4 the backward pass). */
+ * 4 the backward pass, 5 the FP8 backward pass). */
 int sdpa_abi_version(void);
 
 #ifdef __cplusplus

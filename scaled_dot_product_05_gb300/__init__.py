@@ -15,7 +15,7 @@ from . import _abi
 from ._abi import SdpaError, check, lib, status_string
 
 __all__ = ["sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_fwd_decode", "sdpa_fwd_decode_noalloc",
-           "sdpa_bwd", "bwd_workspace_bytes",
+           "sdpa_bwd", "bwd_workspace_bytes", "sdpa_bwd_fp8", "bwd_fp8_workspace_bytes",
            "decode_workspace_bytes", "sdpa_status_string", "sdpa_device_error", "SdpaError", "lib"]
 
 _DTYPE = {torch.bfloat16: _abi.SDPA_DTYPE_BF16, torch.float16: _abi.SDPA_DTYPE_FP16}
@@ -244,6 +244,57 @@ def sdpa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, *, causal: bool = F
                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
                          int(bool(causal)), _DTYPE.get(q.dtype, 99), workspace.data_ptr(),
                          workspace.numel() * workspace.element_size(), _stream_ptr(stream, q.device.index)))
+    return dq, dk, dv
+
+
+def bwd_fp8_workspace_bytes(B: int, Hq: int, Sq: int, D: int) -> int:
+    """Workspace bytes :func:`sdpa_bwd_fp8` needs."""
+    return int(lib().sdpa_bwd_fp8_workspace_bytes(B, Hq, Sq, D))
+
+
+def sdpa_bwd_fp8(q8, k8, v8, o, do8, lse, dq=None, dk=None, dv=None, *, descale_q: float, descale_k: float,
+                 descale_v: float, descale_do: float, scale_ds: float, amax_ds=None, causal: bool = False,
+                 scale: float | None = None, workspace=None, stream=None):
+    """FP8 backward pass: gradients (dq, dk, dv), bf16, of sum(do * o) for
+    o = sdpa_fwd_fp8(q8, k8, v8).  ``q8``, ``k8``, ``v8`` are E4M3 and ``do8``
+    E5M2 (``torch.float8_e4m3fn`` / ``torch.float8_e5m2`` or uint8 codes),
+    contiguous [B, S, H, D] CUDA tensors with per-tensor descales; ``o`` is
+    the forward's bf16 output and ``lse`` its [B, Hq, Sq] float32
+    log-sum-exp.  ``scale_ds`` scales dS before its E5M2 rounding; if
+    ``amax_ds`` (a 1-element float32 CUDA tensor) is given it receives
+    max |dS| of this call.  Outputs and the workspace are allocated when not
+    given."""
+    for t in (q8, k8, v8, do8):
+        if not t.is_cuda or not t.is_contiguous() or t.element_size() != 1:
+            raise ValueError("q8, k8, v8, do8 must be contiguous 1-byte CUDA tensors")
+    B, Hq, Hkv, Sq, Skv, D = _shapes(q8, k8, v8)
+    if tuple(do8.shape) != tuple(q8.shape) or tuple(o.shape) != tuple(q8.shape) or tuple(k8.shape) != tuple(v8.shape):
+        raise ValueError("o and do8 must be shaped like q8, v8 like k8")
+    if not o.is_cuda or not o.is_contiguous() or o.dtype != torch.bfloat16:
+        raise ValueError("o must be a contiguous bf16 CUDA tensor")
+    lse_ptr = _lse_ptr(lse, B, Hq, Sq)
+    if lse_ptr is None:
+        raise ValueError("the forward's lse is required")
+    dq = torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device) if dq is None else dq
+    dk = torch.empty(k8.shape, dtype=torch.bfloat16, device=q8.device) if dk is None else dk
+    dv = torch.empty(v8.shape, dtype=torch.bfloat16, device=q8.device) if dv is None else dv
+    for t, like in ((dq, q8), (dk, k8), (dv, v8)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16 or t.shape != like.shape:
+            raise ValueError("gradients must be contiguous bf16 CUDA tensors shaped like their inputs")
+    amax_ptr = None
+    if amax_ds is not None:
+        if not amax_ds.is_cuda or amax_ds.dtype != torch.float32 or amax_ds.numel() < 1:
+            raise ValueError("amax_ds must be a float32 CUDA tensor")
+        amax_ptr = amax_ds.data_ptr()
+    if workspace is None:
+        workspace = torch.empty(bwd_fp8_workspace_bytes(B, Hq, Sq, D), dtype=torch.uint8, device=q8.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    check(lib().sdpa_bwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), o.data_ptr(), do8.data_ptr(), lse_ptr,
+                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
+                             int(bool(causal)), float(descale_q), float(descale_k), float(descale_v),
+                             float(descale_do), float(scale_ds), amax_ptr, workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), _stream_ptr(stream, q8.device.index)))
     return dq, dk, dv
 
 

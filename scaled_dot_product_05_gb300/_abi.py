@@ -14,7 +14,7 @@ STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_NULL_PTR", 2: "SDPA_ERR_MISALIGNED", 3: "SD
           12: "SDPA_ERR_WORKSPACE"}
 # every function include/sdpa.h declares
 EXPORTS = ("sdpa_fwd", "sdpa_fwd_fp8", "sdpa_fwd_ex", "sdpa_fwd_fp8_ex", "sdpa_fwd_decode",
-           "sdpa_fwd_decode_noalloc", "sdpa_decode_workspace_bytes", "sdpa_bwd", "sdpa_bwd_workspace_bytes", "sdpa_status_string", "sdpa_last_cuda_error", "sdpa_device_error",
+           "sdpa_fwd_decode_noalloc", "sdpa_decode_workspace_bytes", "sdpa_bwd", "sdpa_bwd_workspace_bytes", "sdpa_bwd_fp8", "sdpa_bwd_fp8_workspace_bytes", "sdpa_status_string", "sdpa_last_cuda_error", "sdpa_device_error",
            "sdpa_abi_version")
 
 
@@ -52,6 +52,11 @@ def _bind(lib):
     lib.sdpa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, vp]
     lib.sdpa_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.sdpa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    lib.sdpa_bwd_fp8.restype = i
+    lib.sdpa_bwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, f, f, f, f, f, vp, vp,
+                                 ctypes.c_size_t, vp]
+    lib.sdpa_bwd_fp8_workspace_bytes.restype = ctypes.c_size_t
+    lib.sdpa_bwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
     lib.sdpa_decode_workspace_bytes.restype = ctypes.c_size_t
     lib.sdpa_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
     lib.sdpa_status_string.restype = ctypes.c_char_p

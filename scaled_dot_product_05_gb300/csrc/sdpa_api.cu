@@ -16,6 +16,7 @@
 #include "sdpa_kernel.cuh"
 #include "sdpa_bwd.cuh"
 #include "sdpa_bwd_prep.cuh"
+#include "sdpa_bwd_fp8.cuh"
 
 namespace {
 
@@ -81,6 +82,13 @@ cudaError_t set_bwd_attrs()
                                 sdpa::bwd::BwdLayout<D>::kSmemBytes);
 }
 
+template <int D>
+cudaError_t set_bwd8_attrs()
+{
+    return cudaFuncSetAttribute(sdpa::bwd8::sdpa_bwd_fp8_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                sdpa::bwd8::Layout<D>::kSmemBytes);
+}
+
 sdpa_status_t device_ready(int* dev_out, int* sm_count)
 {
     int dev = 0;
@@ -114,7 +122,8 @@ sdpa_status_t device_ready(int* dev_out, int* sm_count)
                             set_attrs<64, sdpa::kBF16, true>(),  set_attrs<64, sdpa::kFP16, true>(),
                             set_attrs<128, sdpa::kBF16, true>(), set_attrs<128, sdpa::kFP16, true>(),
                             set_bwd_attrs<64, sdpa::kBF16>(),    set_bwd_attrs<64, sdpa::kFP16>(),
-                            set_bwd_attrs<128, sdpa::kBF16>(),   set_bwd_attrs<128, sdpa::kFP16>()};
+                            set_bwd_attrs<128, sdpa::kBF16>(),   set_bwd_attrs<128, sdpa::kFP16>(),
+                            set_bwd8_attrs<64>(),                set_bwd8_attrs<128>()};
         for (cudaError_t x : es)
             if (x != cudaSuccess && st.err == cudaSuccess)
                 st.err = x;
@@ -667,6 +676,121 @@ sdpa_status_t run_bwd(const void* Q, const void* K, const void* V, const void* O
     return SDPA_OK;
 }
 
+// FP8 backward workspace: the fp32 dQ accumulator and Delta as for the
+// 16-bit pass, then one 16-byte word for amax|dS| when the caller passes none.
+size_t bwd8_workspace(int B, int Hq, int Sq, int D)
+{
+    return bwd_workspace(B, Hq, Sq, D) + 16;
+}
+
+template <int D>
+cudaError_t launch_bwd8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                        const CUtensorMap& tdq, const sdpa::bwd8::Params& p, const void* O, const void* dO8, void* dQ,
+                        float dq_factor, cudaStream_t stream)
+{
+    const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
+    cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(float), stream);
+    if (e != cudaSuccess || (e = cudaMemsetAsync(p.amax_ds, 0, sizeof(unsigned int), stream)) != cudaSuccess)
+        return e;
+    constexpr int kRows = 256 / (D / 16);
+    sdpa::bwd8::bwd8_delta_kernel<D, true><<<static_cast<unsigned>((rows + kRows - 1) / kRows), 256, 0, stream>>>(
+        O, dO8, const_cast<float*>(p.delta), p.B, p.Hq, p.Sq);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.n_kt);
+    sdpa::bwd8::sdpa_bwd_fp8_kernel<D>
+        <<<grid, sdpa::bwd::kThreads, sdpa::bwd8::Layout<D>::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    const long long n = rows * D;
+    sdpa::bwd8::bwd8_dq_convert_kernel<<<static_cast<unsigned>((n / 4 + 255) / 256), 256, 0, stream>>>(
+        p.dq_acc, dQ, n, dq_factor);
+    return cudaGetLastError();
+}
+
+sdpa_status_t run_bwd_fp8(const void* Q8, const void* K8, const void* V8, const void* O, const void* dO8,
+                          const float* LSE, void* dQ, void* dK, void* dV, const Shape& s, float scale, int causal,
+                          float descale_q, float descale_k, float descale_v, float descale_do, float scale_ds,
+                          float* amax_ds, void* ws, size_t ws_bytes, void* stream)
+{
+    // Q8, K8, V8, dO8 one byte an element; O, dQ, dK, dV bf16; all contiguous BSHD
+    const Args fwd{Q8, K8, V8, dQ, nullptr, s, contiguous_bshd(s.Sq, s.Hq, s.D), contiguous_bshd(s.Skv, s.Hkv, s.D),
+                   contiguous_bshd(s.Skv, s.Hkv, s.D), contiguous_bshd(s.Sq, s.Hq, s.D)};
+    if (!O || !dO8 || !LSE || !dK || !dV || !ws)
+        return SDPA_ERR_NULL_PTR;
+    sdpa_status_t st = check_common(fwd, 1, 2);      // Q8, K8, V8, dQ: pointers, sizes, heads, dQ vs inputs
+    if (st != SDPA_OK)
+        return st;
+    if (s.D != 64 && s.D != 128)
+        return SDPA_ERR_HEAD_DIM;
+    if (!aligned16(O) || !aligned16(dO8) || !aligned16(dK) || !aligned16(dV) || !aligned16(ws) || !aligned(LSE, 4) ||
+        !aligned(amax_ds, 4))
+        return SDPA_ERR_MISALIGNED;
+    if (!valid_scale(scale) || !valid_scale(descale_q) || !valid_scale(descale_k) || !valid_scale(descale_v) ||
+        !valid_scale(descale_do) || !valid_scale(scale_ds))
+        return SDPA_ERR_SCALE;
+    if (ws_bytes < bwd8_workspace(s.B, s.Hq, s.Sq, s.D))
+        return SDPA_ERR_WORKSPACE;
+    const long long q8_b = static_cast<long long>(s.B) * s.Sq * s.Hq * s.D;
+    const long long kv8_b = static_cast<long long>(s.B) * s.Skv * s.Hkv * s.D;
+    const long long q_b = 2 * q8_b, kv_b = 2 * kv8_b;
+    const long long l_b = static_cast<long long>(s.B) * s.Hq * s.Sq * 4;
+    const long long w_b = static_cast<long long>(bwd8_workspace(s.B, s.Hq, s.Sq, s.D));
+    // every written buffer (dQ, dK, dV, workspace, amax) apart from every other buffer
+    const void* bufs[11] = {Q8, K8, V8, O, dO8, LSE, dQ, dK, dV, ws, amax_ds};
+    const long long lens[11] = {q8_b, kv8_b, kv8_b, q_b, q8_b, l_b, q_b, kv_b, kv_b, w_b, amax_ds ? 4 : 0};
+    for (int w = 6; w < 11; ++w)
+        for (int o = 0; o < 11; ++o)
+            if (o != w && lens[w] > 0 && lens[o] > 0 && overlaps(bufs[w], lens[w], bufs[o], lens[o]))
+                return SDPA_ERR_ALIAS;
+
+    int dev = 0, sm_count = 0;
+    st = device_ready(&dev, &sm_count);
+    if (st != SDPA_OK)
+        return st;
+    float* dq_acc = static_cast<float*>(ws);
+    CUtensorMap tq, tk, tv, tdo, tdq;
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (!make_map(&tq, Q8, u8, 1, s.D, s.Hq, s.Sq, s.B, fwd.q) || !make_map(&tk, K8, u8, 1, s.D, s.Hkv, s.Skv, s.B, fwd.k) ||
+        !make_map(&tv, V8, u8, 1, s.D, s.Hkv, s.Skv, s.B, fwd.v) ||
+        !make_map(&tdo, dO8, u8, 1, s.D, s.Hq, s.Sq, s.B, fwd.q) ||
+        !make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.D, s.Hq, s.Sq, s.B, fwd.q))
+        return cuda_fail(cudaErrorInvalidValue);
+
+    sdpa::bwd8::Params p{};
+    p.lse = LSE;
+    p.dq_acc = dq_acc;
+    p.delta = dq_acc + static_cast<long long>(s.B) * s.Sq * s.Hq * s.D;
+    p.amax_ds = amax_ds ? reinterpret_cast<unsigned int*>(amax_ds)
+                        : reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + bwd_workspace(s.B, s.Hq, s.Sq, s.D));
+    p.dK = dK;
+    p.dV = dV;
+    p.B = s.B;
+    p.Hq = s.Hq;
+    p.Hkv = s.Hkv;
+    p.Sq = s.Sq;
+    p.Skv = s.Skv;
+    p.group = s.Hq / s.Hkv;
+    p.n_qt = (s.Sq + sdpa::kBlockM - 1) / sdpa::kBlockM;
+    p.n_kt = (s.Skv + sdpa::kBlockN - 1) / sdpa::kBlockN;
+    p.causal = causal ? 1 : 0;
+    p.c_s = static_cast<float>(static_cast<double>(scale) * descale_q * descale_k * 1.4426950408889634);
+    p.dv = descale_v;
+    p.ddo = descale_do;
+    p.m_ds = descale_do * scale_ds;
+    p.out_dv = descale_do / sdpa::bwd8::kPScale;
+    p.out_dk = static_cast<float>(static_cast<double>(scale) * descale_q / scale_ds);
+    const float dq_factor = static_cast<float>(static_cast<double>(scale) * descale_k / scale_ds);
+    if (static_cast<long long>(s.B) * s.Hkv * p.n_kt > INT32_MAX)
+        return SDPA_ERR_BAD_SHAPE;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = s.D == 64 ? launch_bwd8<64>(tq, tk, tv, tdo, tdq, p, O, dO8, dQ, dq_factor, cs)
+                                    : launch_bwd8<128>(tq, tk, tv, tdo, tdq, p, O, dO8, dQ, dq_factor, cs);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    return SDPA_OK;
+}
+
 Args make_args(const void* Q, const void* K, const void* V, void* O, float* lse, int B, int Hq, int Hkv, int Sq,
                int Skv, int D, const sdpa_layout_t* ql, const sdpa_layout_t* kl, const sdpa_layout_t* vl,
                const sdpa_layout_t* ol)
@@ -758,6 +882,23 @@ sdpa_status_t sdpa_bwd(const void* Q, const void* K, const void* V, const void* 
                    workspace_bytes, stream);
 }
 
+sdpa_status_t sdpa_bwd_fp8(const void* Q8, const void* K8, const void* V8, const void* O, const void* dO8,
+                           const float* LSE, void* dQ, void* dK, void* dV, int B, int Hq, int Hkv, int Sq, int Skv,
+                           int D, float scale, int causal, float descale_q, float descale_k, float descale_v,
+                           float descale_do, float scale_ds, float* amax_ds, void* workspace, size_t workspace_bytes,
+                           void* stream)
+{
+    return run_bwd_fp8(Q8, K8, V8, O, dO8, LSE, dQ, dK, dV, Shape{B, Hq, Hkv, Sq, Skv, D}, scale, causal, descale_q,
+                       descale_k, descale_v, descale_do, scale_ds, amax_ds, workspace, workspace_bytes, stream);
+}
+
+size_t sdpa_bwd_fp8_workspace_bytes(int B, int Hq, int Sq, int D)
+{
+    if (B < 1 || Hq < 1 || Sq < 1 || (D != 64 && D != 128))
+        return 0;
+    return bwd8_workspace(B, Hq, Sq, D);
+}
+
 size_t sdpa_bwd_workspace_bytes(int B, int Hq, int Sq, int D)
 {
     if (B < 1 || Hq < 1 || Sq < 1 || (D != 64 && D != 128))
@@ -821,7 +962,7 @@ sdpa_status_t sdpa_device_error(unsigned int* code)
 
 int sdpa_abi_version(void)
 {
-    return 4;
+    return 5;
 }
 
 }  // extern "C"

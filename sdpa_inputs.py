@@ -11,6 +11,9 @@ values under a per-tensor scale taken from the absolute maximum (recipe margin
 Generator: ``torch.Generator('cpu').manual_seed(seed)``, then ``randn`` float32
 for Q, K, V in that order, then round-to-nearest-even to bf16 / fp16, or, for
 E4M3, x * (448 / amax(|x|)) rounded to E4M3 with descale = amax / 448.
+Upstream gradients dO for the backward pass: ``randn`` float32 from their own
+seed, rounded to bf16 / fp16, or, in the recipe's gradient format E5M2,
+x * (57344 / amax(|x|)) rounded to E5M2 with descale = amax / 57344.
 """
 from __future__ import annotations
 
@@ -19,6 +22,7 @@ from dataclasses import dataclass
 import torch
 
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
 
 
 @dataclass
@@ -56,6 +60,28 @@ def make_qkv(seed: int, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
     if dtype == "e4m3":
         (q8, dq), (k8, dk), (v8, dv) = _quantise_e4m3(q), _quantise_e4m3(k), _quantise_e4m3(v)
         return QKV(q8, k8, v8, dtype, (dq, dk, dv))
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def _quantise_e5m2(x: torch.Tensor):
+    amax = float(x.abs().max())
+    s = torch.tensor(E5M2_MAX / amax, dtype=torch.float32)
+    x8 = (x * s).to(torch.float8_e5m2)
+    return x8, float(torch.tensor(amax / E5M2_MAX, dtype=torch.float32))
+
+
+def make_grad(seed: int, shape, dtype: str = "bf16"):
+    """Seeded N(0,1) upstream gradient dO (CPU tensor) of ``shape``: a bf16 /
+    fp16 tensor, or for "e5m2" the pair (E5M2 codes, descale)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    x = torch.randn(tuple(shape), generator=g, dtype=torch.float32)
+    if dtype == "bf16":
+        return x.to(torch.bfloat16)
+    if dtype == "fp16":
+        return x.to(torch.float16)
+    if dtype == "e5m2":
+        return _quantise_e5m2(x)
     raise ValueError(f"unknown dtype {dtype!r}")
 
 

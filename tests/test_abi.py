@@ -178,3 +178,61 @@ def test_decode_noalloc_rejects_before_any_cuda_call(lib):
     assert f(QP, KP, VP, OP, None, 1, 12, 4, 1, 1000, 128, None, None, None, None, s(0.1), 0, None) == 4
     assert f(None, KP, VP, OP, None, 1, 8, 2, 1, 1000, 128, None, None, None, None, s(0.1), 0, None) == 1
     assert f(QP, KP, VP, OP, None, 1, 8, 2, 1, 1000, 128, None, None, None, None, s(0.1), 2, None) == 6
+
+
+# the backward entry points: fake, never dereferenced, device addresses far apart
+BP = dict(q=0x10000000, k=0x20000000, v=0x30000000, o=0x40000000, do=0x50000000, lse=0x60000000,
+          dq=0x70000000, dk=0x80000000, dv=0x90000000, ws=0xA0000000, amax=0xB0000000)
+BGOOD = dict(B=2, Hq=8, Hkv=2, Sq=300, Skv=300, D=128, scale=1 / math.sqrt(128), causal=1)
+
+
+def call_bwd(lib, ws_bytes=None, dtype=0, **kw):
+    a = dict(BGOOD, **{k: v for k, v in kw.items() if k in BGOOD})
+    ptr = dict(BP, **{k: v for k, v in kw.items() if k in BP})
+    if ws_bytes is None:
+        ws_bytes = lib.sdpa_bwd_workspace_bytes(a["B"], a["Hq"], a["Sq"], 128)
+    return lib.sdpa_bwd(ptr["q"], ptr["k"], ptr["v"], ptr["o"], ptr["do"], ptr["lse"], ptr["dq"], ptr["dk"],
+                        ptr["dv"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Skv"], a["D"], ctypes.c_float(a["scale"]),
+                        a["causal"], dtype, ptr["ws"], ws_bytes, None)
+
+
+def call_bwd_fp8(lib, ws_bytes=None, descales=(0.01, 0.01, 0.01, 1e-3), scale_ds=1.0, **kw):
+    a = dict(BGOOD, **{k: v for k, v in kw.items() if k in BGOOD})
+    ptr = dict(BP, **{k: v for k, v in kw.items() if k in BP})
+    if ws_bytes is None:
+        ws_bytes = lib.sdpa_bwd_fp8_workspace_bytes(a["B"], a["Hq"], a["Sq"], 128)
+    f = ctypes.c_float
+    return lib.sdpa_bwd_fp8(ptr["q"], ptr["k"], ptr["v"], ptr["o"], ptr["do"], ptr["lse"], ptr["dq"], ptr["dk"],
+                            ptr["dv"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Skv"], a["D"], f(a["scale"]),
+                            a["causal"], *(f(x) for x in descales), f(scale_ds), ptr["amax"], ptr["ws"], ws_bytes,
+                            None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(do=None), 1), (dict(lse=None), 1), (dict(dk=None), 1), (dict(ws=None), 1),
+    (dict(do=BP["do"] + 8), 2), (dict(ws=BP["ws"] + 4), 2),
+    (dict(Sq=0), 3), (dict(Hq=6, Hkv=4), 4), (dict(D=32), 5), (dict(D=96), 5), (dict(dtype=2), 6),
+    (dict(scale=0.0), 7), (dict(ws_bytes=1024), 12),
+    (dict(dq=BP["q"] + 16), 9), (dict(dk=BP["ws"] + 64), 9), (dict(dv=BP["dk"]), 9),
+])
+def test_bwd_rejects_before_any_cuda_call(lib, kw, status):
+    assert call_bwd(lib, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(do=None), 1), (dict(lse=None), 1), (dict(ws=None), 1),
+    (dict(do=BP["do"] + 8), 2), (dict(amax=BP["amax"] + 2), 2), (dict(o=BP["o"] + 8), 2),
+    (dict(Skv=0), 3), (dict(Hq=6, Hkv=4), 4), (dict(D=32), 5), (dict(D=256), 5),
+    (dict(scale=float("nan")), 7), (dict(descales=(0.01, 0.0, 0.01, 1e-3)), 7),
+    (dict(descales=(0.01, 0.01, 0.01, float("inf"))), 7), (dict(scale_ds=0.0), 7), (dict(scale_ds=-2.0), 7),
+    (dict(ws_bytes=4096), 12),
+    (dict(dq=BP["q"] + 16), 9), (dict(amax=BP["ws"] + 64), 9), (dict(dk=BP["dv"]), 9),
+])
+def test_bwd_fp8_rejects_before_any_cuda_call(lib, kw, status):
+    assert call_bwd_fp8(lib, **kw) == status
+
+
+def test_bwd_fp8_workspace_bytes():
+    from scaled_dot_product_05_gb300 import bwd_fp8_workspace_bytes, bwd_workspace_bytes
+    assert bwd_fp8_workspace_bytes(2, 32, 4096, 128) == bwd_workspace_bytes(2, 32, 4096, 128) + 16
+    assert bwd_fp8_workspace_bytes(2, 32, 4096, 32) == 0

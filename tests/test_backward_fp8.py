@@ -1,0 +1,161 @@
+"""GPU parity of the FP8 backward pass (sdpa_bwd_fp8) against the fp64
+oracle's gradients of sum(dO * O) on the dequantised inputs: E4M3 Q, K, V and
+an E5M2 upstream gradient dO (the hybrid recipe of section 10 of the codelab
+"Attention on GPU (cuDNN and TransformerEngine)"), each code times its
+per-tensor descale.  O and the LSE given to the kernel are the oracle's
+forward on the same inputs (O rounded to bf16), so that the comparison
+measures the backward pass alone; one case runs the library's FP8 forward
+pass first, as in training.
+
+Tolerance, from the arithmetic of the kernel.  Rounding to nearest with m
+mantissa bits errs by at most half a unit, 2^-(m+1) of the binade's bottom;
+for values spread evenly over a binade in log scale the mean squared relative
+error is 2^-2(m+1) / 3 * 3 / (8 ln 2), a relative RMS of 2^-(m+1) / sqrt(8 ln 2).
+  * dV = P8^T dO with P8 = e4m3(448 P), m = 3: 2^-4 / 2.355 = 0.027 per term;
+    the errors are independent per term, so dV's relative RMS error over the
+    tensor is about 0.027 (measured 0.025 - 0.027); the test allows 0.04.
+  * dK = scale dS8^T Q and dQ = scale dS8 K with dS8 = e5m2(dS scale_ds),
+    m = 2: 0.053 (measured 0.052 - 0.053); with scale_ds from the amax of an
+    earlier call (the recipe's delayed scaling, margin 0) every |dS| above
+    2^-30 amax stays in E5M2's normal range.  The test allows 0.08.
+  * The rest (fp32 accumulation, exp2 of fp32 scores, bf16 O in Delta and the
+    bf16 outputs, <= 2^-9 relative) is an order below.
+A mistake of layout, format or scale (a transposed operand, E4M3 read as
+E5M2, a descale dropped or applied twice) gives relative errors of order 1.
+The largest single error is also bounded by 0.25 of the tensor's largest
+magnitude (measured <= 0.06).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sdpa_inputs import E5M2_MAX, make_grad, make_qkv
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+TOL = {"dQ": 0.08, "dK": 0.08, "dV": 0.04}
+MAX_FRAC = 0.25
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from scaled_dot_product_05_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+    yield
+    from scaled_dot_product_05_gb300 import sdpa_device_error
+    assert sdpa_device_error() == 0
+
+
+def dequant(t8, descale):
+    return t8.to(torch.float64).numpy() * descale
+
+
+def inputs(shape, seed):
+    B, Hq, Hkv, Sq, Skv, D = shape
+    x = make_qkv(700 + seed, B, Hq, Hkv, Sq, Skv, D, "e4m3")
+    g8, ddo = make_grad(750 + seed, (B, Sq, Hq, D), "e5m2")
+    return x, g8, ddo
+
+
+def run_kernel(x, g8, ddo, o, lse, causal, scale_ds, amax=None):
+    from scaled_dot_product_05_gb300 import sdpa_bwd_fp8
+    dq_, dk_, dv_ = x.descales
+    q8, k8, v8, do8 = (t.to(DEV) for t in (x.q, x.k, x.v, g8))
+    grads = sdpa_bwd_fp8(q8, k8, v8, o, do8, lse, descale_q=dq_, descale_k=dk_, descale_v=dv_, descale_do=ddo,
+                         scale_ds=scale_ds, amax_ds=amax, causal=causal)
+    torch.cuda.synchronize()
+    return [t.float().cpu().double().numpy() for t in grads]
+
+
+def reference(x, g8, ddo, causal):
+    q, k, v = (dequant(t, d) for t, d in zip((x.q, x.k, x.v), x.descales))
+    return oracle.sdpa_backward_reference(q, k, v, dequant(g8, ddo), causal=causal, dtype="f64")
+
+
+def oracle_forward(x, causal):
+    o, lse = oracle.sdpa_reference(x.q, x.k, x.v, causal=causal, dtype="e4m3", descales=x.descales,
+                                   return_lse=True)
+    return (torch.from_numpy(o).to(torch.bfloat16).to(DEV),
+            torch.from_numpy(np.ascontiguousarray(lse)).to(torch.float32).to(DEV))
+
+
+def check(got, ref, what, tol=TOL, max_frac=MAX_FRAC):
+    for name, a, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert np.isfinite(a).all(), f"{what} {name}: non-finite"
+        rms = float(np.linalg.norm(a - r) / max(np.linalg.norm(r), 1e-30))
+        mx = float(np.abs(a - r).max() / max(np.abs(r).max(), 1e-30))
+        print(f"{what} {name}: rel_rms {rms:.3e} max/|ref|max {mx:.3e}")
+        assert rms <= tol[name], f"{what} {name}: rel_rms {rms:.3e} > {tol[name]}"
+        assert mx <= max_frac, f"{what} {name}: max error {mx:.3e} of the largest magnitude"
+
+
+def delayed_scale_run(shape, causal, seed=0):
+    """Two calls as in training: the first with scale_ds = 1 reports
+    amax|dS|, the second uses the recipe's scale E5M2_MAX / amax."""
+    x, g8, ddo = inputs(shape, seed)
+    o, lse = oracle_forward(x, causal)
+    amax = torch.zeros(1, dtype=torch.float32, device=DEV)
+    run_kernel(x, g8, ddo, o, lse, causal, 1.0, amax)
+    a1 = float(amax.item())
+    assert np.isfinite(a1) and a1 > 0
+    got = run_kernel(x, g8, ddo, o, lse, causal, E5M2_MAX / a1, amax)
+    assert float(amax.item()) == a1           # dS does not depend on its scale: the same amax
+    return got, reference(x, g8, ddo, causal)
+
+
+SHAPES = [(1, 4, 2, 300, 300, 128), (2, 4, 4, 257, 257, 64), (1, 8, 1, 256, 384, 128), (1, 4, 2, 200, 330, 64)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_fp8_backward_matches_oracle(shape, causal):
+    got, ref = delayed_scale_run(shape, causal)
+    check(got, ref, f"{shape} causal={causal}")
+
+
+def test_fp8_backward_gqa_1024():
+    got, ref = delayed_scale_run((2, 8, 2, 1024, 1024, 128), True, seed=1)
+    check(got, ref, "gqa 1024 causal")
+
+
+def test_fp8_backward_after_library_forward():
+    # O and the LSE from sdpa_fwd_fp8_ex, as in training; the forward's own
+    # E4M3 rounding of P moves O by <= 6e-2 and the LSE by <= 8e-2 (its
+    # tolerances), which the gradients inherit: allow 0.05 more relative RMS
+    from scaled_dot_product_05_gb300 import sdpa_fwd_fp8_ex
+    shape, causal = (1, 4, 2, 384, 384, 128), True
+    B, Hq, Hkv, Sq, Skv, D = shape
+    x, g8, ddo = inputs(shape, 3)
+    o = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=DEV)
+    dq_, dk_, dv_ = x.descales
+    sdpa_fwd_fp8_ex(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), o, lse, descale_q=dq_, descale_k=dk_, descale_v=dv_,
+                    causal=causal)
+    amax = torch.zeros(1, dtype=torch.float32, device=DEV)
+    run_kernel(x, g8, ddo, o, lse, causal, 1.0, amax)
+    got = run_kernel(x, g8, ddo, o, lse, causal, E5M2_MAX / float(amax.item()))
+    check(got, reference(x, g8, ddo, causal), "after library forward",
+          tol={k: v + 0.05 for k, v in TOL.items()})
+
+
+def test_fp8_dk_dv_deterministic():
+    # dK and dV accumulate in TMEM in a fixed order: bitwise equal across calls
+    x, g8, ddo = inputs((1, 4, 2, 300, 300, 128), 4)
+    o, lse = oracle_forward(x, True)
+    a = run_kernel(x, g8, ddo, o, lse, True, 1024.0)
+    b = run_kernel(x, g8, ddo, o, lse, True, 1024.0)
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+
+
+def test_fp8_zero_gradient_gives_zero():
+    # dO = 0: dP = 0, Delta = 0, so dS = 0 and every gradient is exactly 0
+    x, g8, ddo = inputs((1, 4, 2, 200, 200, 64), 5)
+    g8 = torch.zeros(g8.shape, dtype=torch.uint8).view(torch.float8_e5m2)
+    o, lse = oracle_forward(x, False)
+    for t in run_kernel(x, g8, ddo, o, lse, False, 1.0):
+        assert not np.any(t)
