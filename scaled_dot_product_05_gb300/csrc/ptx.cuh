@@ -439,23 +439,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v)
     return r;
 }
 
-// Two floats -> two E5M2 bytes (round to nearest even, saturate to +-57344):
-// `lo` in the low byte.
-__device__ __forceinline__ uint16_t f32x2_to_e5m2x2(float lo, float hi)
-{
-    uint16_t h;
-    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
-    return h;
-}
-
-// Two E5M2 bytes -> f16x2 (exact: E5M2 is f16 with the low 8 bits cleared).
-__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint16_t v)
-{
-    uint32_t r;
-    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(v));
-    return r;
-}
-
 __device__ __forceinline__ uint32_t add_f16x2(uint32_t a, uint32_t b)
 {
     uint32_t d;

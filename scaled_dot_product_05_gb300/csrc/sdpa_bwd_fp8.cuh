@@ -131,6 +131,23 @@ __host__ __device__ constexpr uint32_t idesc_f8(uint32_t a_fmt, uint32_t b_fmt, 
 }
 constexpr uint32_t kE4M3 = 0, kE5M2 = 1;
 
+// Two floats -> two E5M2 bytes (round to nearest even, saturate to +-57344):
+// `lo` in the low byte.
+__device__ __forceinline__ uint16_t f32x2_to_e5m2x2(float lo, float hi)
+{
+    uint16_t h;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
+    return h;
+}
+
+// Two E5M2 bytes -> f16x2 (exact: E5M2 is f16 with the low 8 bits cleared).
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint16_t v)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
