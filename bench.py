@@ -557,12 +557,15 @@ def run_gpu(args, rank, world, local_rank):
 def oracle_bwd_sample(name, threads=0):
     """Time the fp64 backward oracle on a bounded sample of the workload:
     batch 0, every KV head (the oracle runs one thread per KV head), the
-    first 1024 positions; returns (TFLOP/s, threads, description)."""
+    first S positions, S a multiple of 256 chosen for about 7.5e9 FLOP per
+    thread it gets (10 to 20 s); returns (TFLOP/s, threads, description)."""
     import oracle
     from sdpa_inputs import make_qkv
 
     w = spec(name)
-    S = min(w.Sq, 1024)
+    per_s2 = 10.0 * w.Hq * w.D * (0.5 if w.causal else 1.0)
+    target = 7.5e9 * min(w.Hkv, os.cpu_count() or 1)
+    S = max(256, min(w.Sq, int((target / per_s2) ** 0.5) // 256 * 256))
     x = make_qkv(1000, 1, w.Hq, w.Hkv, S, S, w.D, "bf16")
     do = make_qkv(1001, 1, w.Hq, w.Hkv, S, S, w.D, "bf16").q
     t0 = time.perf_counter()
