@@ -159,3 +159,32 @@ def test_fp8_zero_gradient_gives_zero():
     o, lse = oracle_forward(x, False)
     for t in run_kernel(x, g8, ddo, o, lse, False, 1.0):
         assert not np.any(t)
+
+
+# degenerate shapes (see the 16-bit tests): one query row, one key, exact tile
+# multiples.  Where every visible P is 1, dS = dP - Delta = 0 exactly, but the
+# kernel's Delta comes from the bf16 O, which here is not V (V = E4M3 code x
+# descale needs more than bf16's 8 bits), so dS = -P dDelta with |dDelta| ~
+# 2^-9 |dO||O| / sqrt(D): an absolute dQ / dK error of about 2^-9 sqrt(D)
+# (0.022 at D=128) of the gradients' scale.  Errors are therefore taken
+# relative to max(own norm, 2^-5 x the largest gradient norm).
+EDGE = [(1, 2, 1, 1, 1, 64), (1, 2, 1, 1, 300, 128), (1, 2, 2, 300, 1, 64), (1, 4, 2, 256, 256, 128),
+        (3, 2, 1, 129, 129, 64)]
+
+
+@pytest.mark.parametrize("shape", EDGE, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_fp8_backward_edge_shapes(shape, causal):
+    x, g8, ddo = inputs(shape, 8)
+    o, lse = oracle_forward(x, causal)
+    amax = torch.zeros(1, dtype=torch.float32, device=DEV)
+    run_kernel(x, g8, ddo, o, lse, causal, 1.0, amax)
+    a1 = float(amax.item())
+    got = run_kernel(x, g8, ddo, o, lse, causal, E5M2_MAX / a1 if a1 > 0 else 1.0)
+    ref = reference(x, g8, ddo, causal)
+    scale = max(float(np.linalg.norm(r)) for r in ref)
+    for name, a, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert np.isfinite(a).all(), f"{shape} {name}: non-finite"
+        err = float(np.linalg.norm(a - r)) / max(float(np.linalg.norm(r)), 2.0 ** -5 * scale)
+        print(f"{shape} causal={causal} {name}: rel {err:.3e}")
+        assert err <= TOL[name], f"{shape} {name}: {err:.3e} > {TOL[name]}"
