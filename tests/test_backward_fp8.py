@@ -188,3 +188,37 @@ def test_fp8_backward_edge_shapes(shape, causal):
         err = float(np.linalg.norm(a - r)) / max(float(np.linalg.norm(r)), 2.0 ** -5 * scale)
         print(f"{shape} causal={causal} {name}: rel {err:.3e}")
         assert err <= TOL[name], f"{shape} {name}: {err:.3e} > {TOL[name]}"
+
+
+def test_fp8_backward_full_size_one_head():
+    # the benchmarked FP8 workload at full size (causal MHA B=2 H=16 S=8192
+    # D=128, delayed dS scale from a first call), checked on one (batch,
+    # head): with MHA a head's gradients depend only on its own Q, K, V, dO
+    B, H, S, D = 2, 16, 8192, 128
+    x, g8, ddo = inputs((B, H, H, S, S, D), 9)
+    o, lse = library_fp8_forward(x)
+    amax = torch.zeros(1, dtype=torch.float32, device=DEV)
+    run_kernel(x, g8, ddo, o, lse, True, 1.0, amax)
+    got = run_kernel(x, g8, ddo, o, lse, True, E5M2_MAX / float(amax.item()))
+    b, h = 1, 5
+    dq_, dk_, dv_ = x.descales
+    sl = lambda t: t[b:b + 1, :, h:h + 1].contiguous()
+    q, k, v = (dequant(sl(t), d) for t, d in zip((x.q, x.k, x.v), (dq_, dk_, dv_)))
+    ref = oracle.sdpa_backward_reference(q, k, v, dequant(sl(g8), ddo), causal=True, dtype="f64")
+    check([a[b:b + 1, :, h:h + 1] for a in got], ref, "full size, one head",
+          tol={k: v + 0.05 for k, v in TOL.items()})
+
+
+def library_fp8_forward(x):
+    # O and the LSE for the full-size case come from the library's FP8
+    # forward (the oracle's forward at this size would take minutes); its
+    # rounding of P moves them within the forward's tolerances, which the
+    # 0.05 margin of test_fp8_backward_after_library_forward covers
+    from scaled_dot_product_05_gb300 import sdpa_fwd_fp8_ex
+    B, S, H, D = x.q.shape
+    o = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=DEV)
+    dq_, dk_, dv_ = x.descales
+    sdpa_fwd_fp8_ex(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), o, lse, descale_q=dq_, descale_k=dk_, descale_v=dv_,
+                    causal=True)
+    return o, lse
