@@ -88,7 +88,7 @@ struct BwdBarriers {
     uint64_t q_empty[2];             // Q tile of stage s free (its dQ slices reduced)
     uint64_t do_full[2];             // dO tile of stage s loaded
     uint64_t do_empty[2];            // dO tile of stage s free
-    uint64_t s_full;                 // S^T in TMEM
+    uint64_t s_full[2];              // S^T of tile it in TMEM: barrier it & 1
     uint64_t dp_full;                // dP^T in TMEM
     uint64_t p_ready;                // P^T packed in TMEM (both softmax warpgroups)
     uint64_t ds_ready;               // dS^T packed in TMEM and shared memory
@@ -128,6 +128,11 @@ struct BwdLayout {
     static constexpr int kSmemBytes = kOffBar + 256;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    // D = 64 leaves 128 columns free: S^T alternates between two regions, so
+    // the next tile's S^T needs no wait for this tile's dV MMA
+    static constexpr bool kTwoS = (D == 64);
+    static constexpr uint32_t kColS2 = 384;
+    static_assert(!kTwoS || kColDK + D <= kColS2, "second S^T region");
     static_assert(sizeof(BwdBarriers) <= 256, "barrier block");
     static_assert(D / 32 <= 4, "staging barriers: one per 32-column slice");
     static_assert(kColDK + D <= 512, "TMEM columns");
@@ -191,7 +196,8 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(smem_u32(&bars->do_full[s]), 1);
             mbar_init(smem_u32(&bars->do_empty[s]), 1);
         }
-        mbar_init(smem_u32(&bars->s_full), 1);
+        mbar_init(smem_u32(&bars->s_full[0]), 1);
+        mbar_init(smem_u32(&bars->s_full[1]), 1);
         mbar_init(smem_u32(&bars->dp_full), 1);
         mbar_init(smem_u32(&bars->p_ready), 256);          // both softmax warpgroups
         mbar_init(smem_u32(&bars->ds_ready), 256);
@@ -283,7 +289,8 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t k_lo = (sK >> 4) | kmaj, k_mn = (sK >> 4) | mnmaj;
             const uint32_t v_lo = (sV >> 4) | kmaj;
             const uint32_t ds_lo = (sDS >> 4) | ((uint32_t)(L::kDSChunkBytes >> 4) << 16);
-            const uint32_t s_t = tmem + L::kColS, dp_t = tmem + L::kColDP;
+            const uint32_t dp_t = tmem + L::kColDP;
+            auto s_of = [&](int it) -> uint32_t { return tmem + ((L::kTwoS && (it & 1)) ? L::kColS2 : L::kColS); };
             const uint32_t dv_t = tmem + L::kColDV, dk_t = tmem + L::kColDK;
             // S^T = K Q^T (keys x queries, K = D) of tile `it` into cols 0..127
             auto issue_s = [&](int it) -> bool {
@@ -295,9 +302,9 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int kk = 0; kk < L::kSteps; ++kk) {
                     const uint32_t off = (uint32_t)(((kk * 32 / L::kSwz) * L::kChunkBytes + (kk * 32) % L::kSwz) >> 4);
-                    mma_f16_ss(s_t, desc_join(hi, k_lo + off), desc_join(hi, q_lo + off), id_s, kk > 0);
+                    mma_f16_ss(s_of(it), desc_join(hi, k_lo + off), desc_join(hi, q_lo + off), id_s, kk > 0);
                 }
-                mma_commit(smem_u32(&bars->s_full));
+                mma_commit(smem_u32(&bars->s_full[it & 1]));
                 return true;
             };
             bool ok = wait_bar(smem_u32(&bars->kv_full), 0, abort, kErrBwdWait + 2);
@@ -322,6 +329,15 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mma_f16_ss(dp_t, desc_join(hi, v_lo + off), desc_join(hi, do_lo + off), id_s, kk > 0);
                 }
                 mma_commit(smem_u32(&bars->dp_full));
+                // D = 64: the next tile's S^T into the other region at once if
+                // its Q has landed (that region's last readers, the last tile's
+                // softmax and dV MMA, are done / issued)
+                if (L::kTwoS && !s_next &&
+                    mbar_test_wait(smem_u32(&bars->q_full[(it + 1) & 1]), ((it + 1) >> 1) & 1)) {
+                    if (!(ok = issue_s(it + 1)))
+                        break;
+                    s_next = true;
+                }
                 // dV += P^T dO as soon as P^T is packed: 16 queries per step, P^T
                 // from TMEM (8 columns per step: queries 0..63 in cols 0..31,
                 // 64..127 in cols 64..95), dO MN-major
@@ -333,7 +349,7 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const uint32_t off = (uint32_t)((kk * 16 * L::kSwz) >> 4);
                     const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
                     const uint32_t col = (kk < 4) ? 8 * kk : 32 + 8 * kk;
-                    mma_f16_ts(dv_t, s_t + col, desc_join(hi, do_mn + off), id_o, acc);
+                    mma_f16_ts(dv_t, s_of(it) + col, desc_join(hi, do_mn + off), id_o, acc);
                 }
                 // the next tile's S^T right after this dV MMA (the last reader of
                 // cols 0..127) if its Q has landed: it runs while the softmax
@@ -437,13 +453,14 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int kr = quarter * 32 + lane;                 // key row of the tile (= TMEM lane)
         const int key = kt * kBlockN + kr;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-        const uint32_t s_t = tmem + lane_addr + L::kColS;
         const uint32_t dp_t = tmem + lane_addr + L::kColDP;
         const float c = p.scale_log2;
         const bool key_ok = key < p.Skv;
         bool ok = true;
         for (int it = 0; ok && it < n_iter; ++it) {
-            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full), it & 1, abort, kErrBwdWait + 6));
+            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_full[it & 1]), (it >> 1) & 1, abort,
+                                                  kErrBwdWait + 6));
+            const uint32_t s_t = tmem + lane_addr + ((L::kTwoS && (it & 1)) ? L::kColS2 : L::kColS);
             if (ok)
                 ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->stats_full[it & 1]), (it >> 1) & 1, abort,
                                                       kErrBwdWait + 9));
