@@ -11,17 +11,22 @@
 //
 // One CTA per (batch, KV head, key tile of 128 keys) owns dK and dV of its
 // keys and loops over the query tiles (causal: those on or below its keys)
-// of every query head of the group, accumulating in TMEM:
-//   warp 0       TMA producer: K, V once; Q and dO tiles into a 2-stage ring
+// of every query head of the group, accumulating in TMEM; key tiles vary
+// slowest over the grid, so the longest CTAs start first:
+//   warp 0       TMA producer: K, V once; Q and dO tiles into a 2-stage ring,
+//                  each with its own full / empty barriers
+//   warp 1       tcgen05 issue, per query tile: S^T = K Q^T (cols 0..127;
+//                  at D = 64 alternately cols 384..511), dP^T = V dO^T
+//                  (cols 128..255); dV += P^T dO once P^T is packed, dK +=
+//                  dS^T Q once dS^T is (both read from TMEM); dQ_part = dS K
+//                  (dS from shared memory, an MN-major A operand) into cols
+//                  128..128+D-1.  The next tile's S^T goes in as early as its
+//                  columns and its Q allow
 //   warp 2       dQ reducer: adds the staged dQ_part of a query tile into
 //                  the fp32 dQ accumulator in HBM (TMA bulk reductions), then
-//                  hands the tile's Q / dO stage back to the producer
-//   warp 1       tcgen05 issue, per query tile: S^T = K Q^T (cols 0..127),
-//                  dP^T = V dO^T (cols 128..255); dV += P^T dO once P^T is
-//                  packed, dK += dS^T Q once dS^T is (both read from TMEM);
-//                  dQ_part = dS K (dS from shared memory, an MN-major A
-//                  operand) into cols 128..128+D-1, so the next tile's S^T
-//                  needs no wait for the dQ warps
+//                  hands the tile's Q, then dO, back to the producer
+//   warp 3       statistics: LSE2 = LSE log2(e) and Delta of the next tile
+//                  into a double-buffered shared array
 //   warps 4..11  two warpgroups, one thread per key row each, the first for
 //                  queries 0..63 of the tile, the second for 64..127: first
 //                  P^T = exp2(S^T c - LSE2) (from S^T alone), then dS^T =
