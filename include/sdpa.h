@@ -200,7 +200,11 @@ sdpa_status_t sdpa_fwd_decode_noalloc(const void *Q, const void *K, const void *
 
 /*
  * Backward pass (bf16 / fp16, contiguous BSHD, D 64 or 128): the gradients of
- * sum(dO * O) for O = sdpa_fwd(Q, K, V) with the same scale and mask.
+ * sum(dO * O) for O = sdpa_fwd(Q, K, V) with the same scale and mask -- the
+ * chain rule applied to section 1's definition (P = exp(S - LSE), dV = P^T dO,
+ * dP = dO V^T, Delta_i = dO_i . O_i, dS = P * (dP - Delta), dQ = scale dS K,
+ * dK = scale dS^T Q); section 10 names the backward pass as what training
+ * runs.
  *   Q, K, V   the forward's inputs; O its output; dO the upstream gradient
  *             (shaped and typed like O); LSE the forward's log-sum-exp
  *             (fp32 [B][Hq][Sq], from sdpa_fwd_ex).  All device, read only.
