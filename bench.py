@@ -168,13 +168,15 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
+    PERIOD_MS = 10
+
     def __init__(self, index):
         self.samples = []
         self.proc = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
@@ -201,7 +203,7 @@ class ClockSampler:
             # region shorter than the sampling period: nearest samples under load
             near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
             inside = [p for _, p in near]
-            note = "timed region shorter than the 50 ms sampling period; nearest samples"
+            note = f"no sample inside the timed region ({self.PERIOD_MS} ms sampling period); nearest samples"
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
 
