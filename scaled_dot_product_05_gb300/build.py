@@ -10,15 +10,20 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libsdpa_gb300.so")
 SOURCES = ["sdpa_api.cu"]
-HEADERS = ["sdpa_kernel.cuh", "sdpa_bwd.cuh", "sdpa_bwd_prep.cuh", "ptx.cuh"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-shared"]
 
 
+def headers():
+    """Every header the library's sources can include: all of csrc/*.cuh and
+    the public headers under include/."""
+    inc = os.path.join(ROOT, "include")
+    return sorted([os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))] +
+                  [os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h")])
+
+
 def _inputs():
-    files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    files.append(os.path.join(ROOT, "include", "sdpa.h"))
-    return files
+    return [os.path.join(CSRC, f) for f in SOURCES] + headers()
 
 
 def up_to_date() -> bool:
