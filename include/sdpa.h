@@ -25,7 +25,9 @@
  * O are device pointers (cudaMalloc / PyTorch CUDA tensors) except where a
  * function says otherwise.  The library allocates no device memory.  Work is
  * enqueued on `stream` (a cudaStream_t; NULL means the legacy default stream)
- * and the call returns without synchronising.
+ * and the call returns without synchronising.  Every call works on the
+ * calling thread's current CUDA device: the buffers and the stream must
+ * belong to it.
  *
  * Errors.  Every argument is checked before any CUDA call; on a failed check
  * the function returns a status code, enqueues nothing and leaves O
@@ -182,8 +184,18 @@ sdpa_status_t sdpa_fwd_decode(const void *Q, const void *K, const void *V, void 
  * sdpa_fwd_decode without a caller workspace and without allocating: the
  * split results go to a 32 MiB scratch array that the library holds in
  * device memory (one per device, part of the loaded module).  The codelab
- * has no counterpart to this entry point; it exists for callers that cannot
- * allocate or pass a workspace.
+ * has no counterpart to this entry point.  It exists for callers that cannot
+ * allocate or pass a workspace: a plugin or kernel hook that receives only
+ * the tensors from a host framework that owns the allocator, code that must
+ * not call cudaMalloc / cudaFree because they synchronise the device (a
+ * latency-bound decode loop), or a caller with no free device memory to
+ * spare at that point.
+ *   - Cost: the module's scratch is reserved on every device where the
+ *     library is loaded, by every process that uses it, even one that never
+ *     calls this function.
+ *   - Set-up: the first call on a device looks up the scratch's device
+ *     address (cudaGetSymbolAddress, once per device, on the current device);
+ *     make that first call before any stream capture.
  *   - Plans that would need more than the scratch return SDPA_ERR_WORKSPACE
  *     (none do on a device with <= 240 SMs at D <= 128).
  *   - Nothing in the scratch has to start at zero: each call writes every

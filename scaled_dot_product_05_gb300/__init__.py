@@ -34,6 +34,18 @@ def _stream_ptr(stream, device_index: int):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _run(device_index: int, fn, *args) -> None:
+    """Call ``fn`` with the tensors' device current: the C library works on
+    the current CUDA device (its SM count, kernel attributes and the decode
+    scratch are per device), so a call on tensors of another device switches
+    to it for the duration of the call."""
+    if torch.cuda.current_device() != device_index:
+        with torch.cuda.device(device_index):
+            check(fn(*args))
+    else:
+        check(fn(*args))
+
+
 def _shapes(q, k, v):
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("Q, K, V must be [B, S, H, D]")
@@ -63,8 +75,8 @@ def sdpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor 
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     dt = _DTYPE.get(q.dtype, 99)
-    check(lib().sdpa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
-                         float(scale), int(bool(causal)), dt, _stream_ptr(stream, q.device.index)))
+    _run(q.device.index, lib().sdpa_fwd, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
+                         float(scale), int(bool(causal)), dt, _stream_ptr(stream, q.device.index))
     return o
 
 
@@ -83,9 +95,9 @@ def sdpa_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Ten
         raise ValueError("o must be a contiguous bf16 CUDA tensor shaped like q")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    check(lib().sdpa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
+    _run(q.device.index, lib().sdpa_fwd_fp8, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), B, Hq, Hkv, Sq, Skv, D,
                              float(scale), float(descale_q), float(descale_k), float(descale_v),
-                             int(bool(causal)), _stream_ptr(stream, q.device.index)))
+                             int(bool(causal)), _stream_ptr(stream, q.device.index))
     return o
 
 
@@ -121,10 +133,10 @@ def sdpa_fwd_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tens
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     lq, lk, lv, lo = _layout(q), _layout(k), _layout(v), _layout(o)
-    check(lib().sdpa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _lse_ptr(lse, B, Hq, Sq),
+    _run(q.device.index, lib().sdpa_fwd_ex, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _lse_ptr(lse, B, Hq, Sq),
                             B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq), ctypes.byref(lk), ctypes.byref(lv),
                             ctypes.byref(lo), float(scale), int(bool(causal)), _DTYPE.get(q.dtype, 99),
-                            _stream_ptr(stream, q.device.index)))
+                            _stream_ptr(stream, q.device.index))
     return o
 
 
@@ -143,10 +155,10 @@ def sdpa_fwd_fp8_ex(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     lq, lk, lv, lo = _layout(q), _layout(k), _layout(v), _layout(o)
-    check(lib().sdpa_fwd_fp8_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _lse_ptr(lse, B, Hq, Sq),
+    _run(q.device.index, lib().sdpa_fwd_fp8_ex, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _lse_ptr(lse, B, Hq, Sq),
                                 B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq), ctypes.byref(lk), ctypes.byref(lv),
                                 ctypes.byref(lo), float(scale), float(descale_q), float(descale_k),
-                                float(descale_v), int(bool(causal)), _stream_ptr(stream, q.device.index)))
+                                float(descale_v), int(bool(causal)), _stream_ptr(stream, q.device.index))
     return o
 
 
@@ -180,10 +192,10 @@ def sdpa_fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.
             raise ValueError("workspace must be a contiguous CUDA tensor")
         ws, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     lq, lk, lv, lo = _layout(q), _layout(k), _layout(v), _layout(o)
-    check(lib().sdpa_fwd_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _lse_ptr(lse, B, Hq, Sq),
+    _run(q.device.index, lib().sdpa_fwd_decode, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), _lse_ptr(lse, B, Hq, Sq),
                                 B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq), ctypes.byref(lk), ctypes.byref(lv),
                                 ctypes.byref(lo), float(scale), _DTYPE.get(q.dtype, 99), ws, ws_bytes,
-                                _stream_ptr(stream, q.device.index)))
+                                _stream_ptr(stream, q.device.index))
     return o
 
 
@@ -203,10 +215,10 @@ def sdpa_fwd_decode_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     lq, lk, lv, lo = _layout(q), _layout(k), _layout(v), _layout(o)
-    check(lib().sdpa_fwd_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+    _run(q.device.index, lib().sdpa_fwd_decode_noalloc, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                         _lse_ptr(lse, B, Hq, Sq), B, Hq, Hkv, Sq, Skv, D, ctypes.byref(lq),
                                         ctypes.byref(lk), ctypes.byref(lv), ctypes.byref(lo), float(scale),
-                                        _DTYPE.get(q.dtype, 99), _stream_ptr(stream, q.device.index)))
+                                        _DTYPE.get(q.dtype, 99), _stream_ptr(stream, q.device.index))
     return o
 
 
@@ -240,10 +252,10 @@ def sdpa_bwd(q, k, v, o, do, lse, dq=None, dk=None, dv=None, *, causal: bool = F
         workspace = torch.empty(bwd_workspace_bytes(B, Hq, Sq, D), dtype=torch.uint8, device=q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    check(lib().sdpa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse_ptr,
+    _run(q.device.index, lib().sdpa_bwd, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse_ptr,
                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
                          int(bool(causal)), _DTYPE.get(q.dtype, 99), workspace.data_ptr(),
-                         workspace.numel() * workspace.element_size(), _stream_ptr(stream, q.device.index)))
+                         workspace.numel() * workspace.element_size(), _stream_ptr(stream, q.device.index))
     return dq, dk, dv
 
 
@@ -290,11 +302,11 @@ def sdpa_bwd_fp8(q8, k8, v8, o, do8, lse, dq=None, dk=None, dv=None, *, descale_
         workspace = torch.empty(bwd_fp8_workspace_bytes(B, Hq, Sq, D), dtype=torch.uint8, device=q8.device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    check(lib().sdpa_bwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), o.data_ptr(), do8.data_ptr(), lse_ptr,
+    _run(q8.device.index, lib().sdpa_bwd_fp8, q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), o.data_ptr(), do8.data_ptr(), lse_ptr,
                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Sq, Skv, D, float(scale),
                              int(bool(causal)), float(descale_q), float(descale_k), float(descale_v),
                              float(descale_do), float(scale_ds), amax_ptr, workspace.data_ptr(),
-                             workspace.numel() * workspace.element_size(), _stream_ptr(stream, q8.device.index)))
+                             workspace.numel() * workspace.element_size(), _stream_ptr(stream, q8.device.index))
     return dq, dk, dv
 
 

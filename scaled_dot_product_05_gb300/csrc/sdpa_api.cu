@@ -23,7 +23,9 @@ namespace {
 thread_local int t_last_cuda_error = 0;
 
 // Scratch of sdpa_fwd_decode_noalloc: a file-scope device array (one instance
-// per device, allocated with the module, never by a call).  A split plan
+// per device, allocated with the module, never by a call; every process that
+// loads the library holds these 32 MiB on each device it uses, whichever entry
+// points it calls).  A split plan
 // needs at most rows * splits * (D + 1) * 4 bytes with B * Hkv * pairs *
 // splits <= #SMs, i.e. #SMs * 256 * 129 * 4 bytes (about 20 MB on 152 SMs);
 // larger plans are rejected.  Nothing in it needs to start at zero: every
@@ -65,6 +67,10 @@ struct DeviceState {
     cudaError_t err = cudaSuccess;
     bool arch_ok = false;
     int sm_count = 0;
+    // this device's instance of g_decode_scratch, looked up once
+    std::once_flag scratch_once;
+    cudaError_t scratch_err = cudaSuccess;
+    void* scratch = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -134,6 +140,20 @@ sdpa_status_t device_ready(int* dev_out, int* sm_count)
         return SDPA_ERR_ARCH;
     *dev_out = dev;
     *sm_count = st.sm_count;
+    return SDPA_OK;
+}
+
+// Device address of the current device's g_decode_scratch.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current, as device_ready leaves it) and
+// kept.
+sdpa_status_t decode_scratch(int dev, void** out)
+{
+    DeviceState& st = g_dev[dev];
+    std::call_once(st.scratch_once, [&] { st.scratch_err = cudaGetSymbolAddress(&st.scratch, g_decode_scratch); });
+    if (st.scratch_err != cudaSuccess)
+        return cuda_fail(st.scratch_err);
+    *out = st.scratch;
     return SDPA_OK;
 }
 
@@ -303,7 +323,7 @@ struct MapKey {
 };
 
 struct MapCache {
-    static constexpr int kSize = 12;
+    static constexpr int kSize = 32;
     MapKey key[kSize];
     CUtensorMap map[kSize];
     bool used[kSize] = {};
@@ -348,13 +368,13 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
 }
 
 template <int D, int KIND, bool kPacked = false>
-cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const sdpa::Params& p,
-                   int sm_count, cudaStream_t stream)
+cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                   const sdpa::Params& p, int sm_count, cudaStream_t stream)
 {
     // persistent: one CTA per SM (each takes all 512 TMEM columns)
     const unsigned grid = static_cast<unsigned>(p.n_units < sm_count ? p.n_units : sm_count);
     sdpa::sdpa_fwd_kernel<D, KIND, kPacked>
-        <<<grid, sdpa::kThreads, sdpa::Layout<D, KIND>::kSmemBytes, stream>>>(tq, tk, tv, p);
+        <<<grid, sdpa::kThreads, sdpa::Layout<D, KIND>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
     cudaError_t e = cudaGetLastError();
     if constexpr (kPacked) {
         if (e == cudaSuccess && p.part_o) {
@@ -394,15 +414,15 @@ sdpa::Params make_params(const Args& a, double score_scale, float out_scale, int
 
 template <int KIND>
 cudaError_t launch_kind(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const sdpa::Params& p, int sm_count, cudaStream_t stream)
+                        const CUtensorMap& to, const sdpa::Params& p, int sm_count, cudaStream_t stream)
 {
     if (D == 32) {
         if constexpr (KIND != sdpa::kE4M3)
-            return launch<32, KIND>(tq, tk, tv, p, sm_count, stream);
+            return launch<32, KIND>(tq, tk, tv, to, p, sm_count, stream);
         return cudaErrorInvalidValue;           // rejected by check_common
     }
-    return D == 64 ? launch<64, KIND>(tq, tk, tv, p, sm_count, stream)
-                   : launch<128, KIND>(tq, tk, tv, p, sm_count, stream);
+    return D == 64 ? launch<64, KIND>(tq, tk, tv, to, p, sm_count, stream)
+                   : launch<128, KIND>(tq, tk, tv, to, p, sm_count, stream);
 }
 
 // The forward pass for already resolved arguments: checks, tensor maps,
@@ -439,17 +459,21 @@ sdpa_status_t run(const Args& a, float scale, const float* descales, int causal,
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                  : dtype == SDPA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap tq, tk, tv;
+    // O is written by TMA stores of 32 rows per softmax warp
+    const CUtensorMapDataType dt_o = dtype == SDPA_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tq, tk, tv, to;
     if (!make_map(&tq, a.Q, dt, in_bytes, s.D, s.Hq, s.Sq, s.B, a.q) ||
         !make_map(&tk, a.K, dt, in_bytes, s.D, s.Hkv, s.Skv, s.B, a.k) ||
-        !make_map(&tv, a.V, dt, in_bytes, s.D, s.Hkv, s.Skv, s.B, a.v))
+        !make_map(&tv, a.V, dt, in_bytes, s.D, s.Hkv, s.Skv, s.B, a.v) ||
+        !make_map(&to, a.O, dt_o, 2, s.D, s.Hq, s.Sq, s.B, a.o, 1, 32))
         return cuda_fail(cudaErrorInvalidValue);
 
     const sdpa::Params p = make_params(a, score_scale, out_scale, causal);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = fp8 ? launch_kind<sdpa::kE4M3>(s.D, tq, tk, tv, p, sm_count, cs)
-                        : dtype == SDPA_DTYPE_BF16 ? launch_kind<sdpa::kBF16>(s.D, tq, tk, tv, p, sm_count, cs)
-                                                   : launch_kind<sdpa::kFP16>(s.D, tq, tk, tv, p, sm_count, cs);
+    const cudaError_t e = fp8 ? launch_kind<sdpa::kE4M3>(s.D, tq, tk, tv, to, p, sm_count, cs)
+                        : dtype == SDPA_DTYPE_BF16 ? launch_kind<sdpa::kBF16>(s.D, tq, tk, tv, to, p, sm_count, cs)
+                                                   : launch_kind<sdpa::kFP16>(s.D, tq, tk, tv, to, p, sm_count, cs);
     if (e != cudaSuccess)
         return cuda_fail(e);
     return SDPA_OK;
@@ -547,15 +571,17 @@ sdpa_status_t run_decode(const Args& a, float scale, sdpa_dtype_t dtype, void* w
         p.part_lse = p.part_o + rows * d.n_splits * s.D;
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    CUtensorMap unused;                  // packed mode writes O with plain stores
+    std::memset(&unused, 0, sizeof unused);
     cudaError_t e;
     if (dtype == SDPA_DTYPE_BF16)
-        e = s.D == 32 ? launch<32, sdpa::kBF16, true>(tq, tk, tv, p, sm_count, cs)
-          : s.D == 64 ? launch<64, sdpa::kBF16, true>(tq, tk, tv, p, sm_count, cs)
-                      : launch<128, sdpa::kBF16, true>(tq, tk, tv, p, sm_count, cs);
+        e = s.D == 32 ? launch<32, sdpa::kBF16, true>(tq, tk, tv, unused, p, sm_count, cs)
+          : s.D == 64 ? launch<64, sdpa::kBF16, true>(tq, tk, tv, unused, p, sm_count, cs)
+                      : launch<128, sdpa::kBF16, true>(tq, tk, tv, unused, p, sm_count, cs);
     else
-        e = s.D == 32 ? launch<32, sdpa::kFP16, true>(tq, tk, tv, p, sm_count, cs)
-          : s.D == 64 ? launch<64, sdpa::kFP16, true>(tq, tk, tv, p, sm_count, cs)
-                      : launch<128, sdpa::kFP16, true>(tq, tk, tv, p, sm_count, cs);
+        e = s.D == 32 ? launch<32, sdpa::kFP16, true>(tq, tk, tv, unused, p, sm_count, cs)
+          : s.D == 64 ? launch<64, sdpa::kFP16, true>(tq, tk, tv, unused, p, sm_count, cs)
+                      : launch<128, sdpa::kFP16, true>(tq, tk, tv, unused, p, sm_count, cs);
     if (e != cudaSuccess)
         return cuda_fail(e);
     return SDPA_OK;
@@ -867,10 +893,13 @@ sdpa_status_t sdpa_fwd_decode_noalloc(const void* Q, const void* K, const void* 
     if (sdpa::kBlockM % (Hq / Hkv) != 0)
         return SDPA_ERR_HEADS;
     // the current device's instance of the library's scratch array
+    int dev = 0, sm_count = 0;
+    sdpa_status_t ds = device_ready(&dev, &sm_count);
     void* scratch = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&scratch, g_decode_scratch);
-    if (e != cudaSuccess)
-        return cuda_fail(e);
+    if (ds == SDPA_OK)
+        ds = decode_scratch(dev, &scratch);
+    if (ds != SDPA_OK)
+        return ds;
     return run_decode(a, scale, dtype, scratch, kDecodeScratchBytes, stream);
 }
 

@@ -124,8 +124,10 @@ struct Layout {
     static constexpr int kSSteps = kRowBytes / 32;                     // S MMAs: 32 bytes of K each
     static constexpr int kKeysPerStep = 32 / kEsize;                   // P V MMAs: 16 (16-bit) or 32 (8-bit) keys
     static constexpr int kPVSteps = kBlockN / kKeysPerStep;
-    static constexpr int kStagesK = (kTileBytes >= 32768) ? 3 : 4;
-    static constexpr int kStagesV = (kTileBytes >= 32768) ? 2 : 4;
+    // 16-bit D = 128 keeps 2 K stages, E4M3 D = 128 3 V stages, so that the
+    // output staging below fits
+    static constexpr int kStagesK = (kTileBytes >= 32768) ? 2 : 4;
+    static constexpr int kStagesV = (kTileBytes >= 32768) ? 2 : (KIND == kE4M3 && D == 128) ? 3 : 4;
     static constexpr int kOffQ = 0;                                    // Q tile 0, Q tile 1
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
@@ -137,7 +139,16 @@ struct Layout {
     static constexpr int kOnesBytes = 16 * kBlockN;
     static constexpr int kOffP = kOffV + kStagesV * kTileBytes;
     static constexpr int kOffOnes = kOffP + 2 * kPTileBytes;
-    static constexpr int kOffBar = (KIND == kE4M3) ? kOffOnes + kOnesBytes : kOffP;
+    // Output staging: each softmax warp writes its 32 rows of O (16-bit,
+    // bf16 for E4M3 inputs) here, one swizzle span (kOSwz bytes) of every row
+    // per pass, and a TMA tensor store moves them to HBM in whole lines.
+    static constexpr int kORowBytes = D * 2;
+    static constexpr int kOSwz = kORowBytes < 128 ? kORowBytes : 128;
+    static constexpr int kOPasses = kORowBytes / kOSwz;
+    static constexpr int kOWarpBytes = 32 * kOSwz;
+    static constexpr int kOffO = (KIND == kE4M3) ? kOffOnes + kOnesBytes : kOffP;
+    static_assert(kOffO % 1024 == 0, "output staging must sit on a swizzle-atom boundary");
+    static constexpr int kOffBar = kOffO + 8 * kOWarpBytes;
     static constexpr int kBarBytes = 1024;
     static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;     // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -482,10 +493,12 @@ __device__ __forceinline__ void mma_issue_pv(const Params& p, Barriers<NK, NV>* 
     drain_wait(smem_u32(&bars->drain[t]), 0);
 }
 
+// tm_o: O as [B][Sq][Hq][D] with the caller's strides, box {kOSwz bytes of a
+// row, 1 head, 32 rows, 1 batch}; unused in packed mode.
 template <int D, int KIND, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
 sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const Params p)
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const Params p)
 {
     using L = Layout<D, KIND>;
     constexpr bool kFP8 = (KIND == kE4M3);
@@ -504,6 +517,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t sK = smem_u32(smem + L::kOffK);
     const uint32_t sV = smem_u32(smem + L::kOffV);
     const uint32_t sP = smem_u32(smem + L::kOffP);     // E4M3 only
+    const uint32_t sO = smem_u32(smem + L::kOffO);     // output staging
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
@@ -535,6 +549,8 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_prefetch_map(&tm_q);
         tma_prefetch_map(&tm_k);
         tma_prefetch_map(&tm_v);
+        if constexpr (!kPacked)
+            tma_prefetch_map(&tm_o);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&bars->tmem_base), L::kTmemCols);
@@ -818,38 +834,79 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 l = __uint_as_float(tmem_ld1_wait(l_tmem));   // sum of the E4M3 P values (tensor core, fp32)
             tc_fence_before_sync();
             mbar_arrive(smem_u32(&bars->o_empty[t]));
-            if (q_idx < p.Sq) {
-                const float inv_l = p.out_scale / l;
+            const float inv_l = p.out_scale / l;
+            const int64_t row_id = ((int64_t)w.b * p.Hq + hq) * p.Sq + q_idx;
+            if (q_idx < p.Sq && (p.lse || (kPacked && p.part_o))) {
                 // log sum_j exp(s_j) = ln 2 * (m + log2 l): m is the max of
                 // s * log2(e) the weights were taken against, l their sum
                 // (E4M3: of the weights times 56)
                 const float lse = (m + (kFP8 ? log2f(l) - kLog2P8Scale : log2f(l))) * kLn2;
-                const int64_t row_id = ((int64_t)w.b * p.Hq + hq) * p.Sq + q_idx;
-                if (kPacked && p.part_o) {
-                    // one split of the key range: O / l in fp32 and the LSE, merged later
-                    const int64_t slot = row_id * p.n_splits + w.split;
-                    p.part_lse[slot] = lse;
-                    float4* dst = reinterpret_cast<float4*>(p.part_o + slot * D);
+                if (kPacked && p.part_o)
+                    p.part_lse[row_id * p.n_splits + w.split] = lse;
+                else
+                    p.lse[row_id] = lse;
+            }
+            if constexpr (kPacked) {
+                if (q_idx < p.Sq) {
+                    if (p.part_o) {
+                        // one split of the key range: O / l in fp32, merged later
+                        float4* dst = reinterpret_cast<float4*>(p.part_o + (row_id * p.n_splits + w.split) * D);
 #pragma unroll
-                    for (int v = 0; v < D / 4; ++v)
-                        dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                             __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
-                } else {
-                    if (p.lse)
-                        p.lse[row_id] = lse;
-                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.O) +
-                                                          ((int64_t)w.b * p.o_sb + (int64_t)q_idx * p.o_ss +
-                                                           (int64_t)hq * p.o_sh) * 2);
+                        for (int v = 0; v < D / 4; ++v)
+                            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                                 __uint_as_float(o[4 * v + 2]) * inv_l,
+                                                 __uint_as_float(o[4 * v + 3]) * inv_l);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.O) +
+                                                              ((int64_t)w.b * p.o_sb + (int64_t)q_idx * p.o_ss +
+                                                               (int64_t)hq * p.o_sh) * 2);
 #pragma unroll
-                    for (int v = 0; v < D / 8; ++v)
-                        dst[v] = make_uint4(pack2<kOutBF16>(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
-                                            pack2<kOutBF16>(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l),
-                                            pack2<kOutBF16>(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l),
-                                            pack2<kOutBF16>(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l));
+                        for (int v = 0; v < D / 8; ++v)
+                            dst[v] = make_uint4(
+                                pack2<kOutBF16>(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l),
+                                pack2<kOutBF16>(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l),
+                                pack2<kOutBF16>(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l),
+                                pack2<kOutBF16>(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l));
+                    }
+                }
+            } else {
+                // O / l -> 16-bit rows of this warp in its staging area (row
+                // = lane, 16-byte units swizzled as the TMA store reads them:
+                // unit u of row r at u ^ (r & 7), or u ^ ((r >> 1) & 3) for
+                // 64-byte rows), then one TMA store per pass.  Rows past Sq
+                // are clipped by the store.
+                const uint32_t stage = sO + (uint32_t)warp * L::kOWarpBytes;
+                const int q_warp = w.pair * kUnitRows + t * kBlockM + quarter * 32;   // first row of the warp
+                constexpr int kUnits = L::kOSwz / 16;
+                const uint32_t swz = (L::kOSwz == 128) ? (uint32_t)(lane & 7) : (uint32_t)((lane >> 1) & 3);
+#pragma unroll
+                for (int c = 0; c < L::kOPasses; ++c) {
+                    // the previous store from this staging area has read it
+                    if (lane == 0)
+                        bulk_wait_group_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int u = 0; u < kUnits; ++u) {
+                        const int e = c * (L::kOSwz / 2) + 8 * u;      // first of the unit's 8 elements
+                        st_shared_v4(stage + (uint32_t)(lane * L::kOSwz) + (((uint32_t)u ^ swz) << 4),
+                                     pack2<kOutBF16>(__uint_as_float(o[e + 0]) * inv_l, __uint_as_float(o[e + 1]) * inv_l),
+                                     pack2<kOutBF16>(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l),
+                                     pack2<kOutBF16>(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l),
+                                     pack2<kOutBF16>(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l));
+                    }
+                    fence_proxy_async_smem();                  // visible to the TMA engine
+                    __syncwarp();
+                    if (lane == 0 && q_warp < p.Sq) {
+                        tma_store_4d(&tm_o, stage, c * (L::kOSwz / 2), hq, q_warp, w.b);
+                        bulk_commit_group();
+                    }
                 }
             }
             ++units;
         }
+        // every output store has completed before the CTA exits
+        if (!kPacked && lane == 0)
+            bulk_wait_group0();
     }
 
     tc_fence_before_sync();
