@@ -138,6 +138,50 @@ def kernel_source_hash(name=None):
     return h.hexdigest()[:16]
 
 
+# NVIDIA's nominal dense figures for one GB300 GPU (context beside the measured
+# peaks): bf16 2.25 PFLOP/s, FP8 4.5 PFLOP/s, HBM3e ~7.9 TB/s
+NOMINAL = {"bf16_tflops": 2250.0, "fp8_tflops": 4500.0, "hbm_gbs": 7900.0}
+# the headline's timed region (K steps) is repeated until the repeats add up to
+# about this long, so that the clock sampler sees the kernel under load
+TIMED_TARGET_MS = 300.0
+
+
+def cpu_model() -> str:
+    """Host CPU model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def workload_config(name, world, **extra):
+    """The `config` object of a bench line: the workload by name and sizes
+    (identical keys for the GPU arm and the reference arm)."""
+    w = spec(name)
+    kind = "backward pass, " if name in BWD_WORKLOADS else ""
+    cfg = {"workload": kind + describe(name), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Skv": w.Skv, "D": w.D,
+           "causal": w.causal, "flops_per_step": step_flops(name), "parallelism": f"replicas x{world}"}
+    cfg.update(extra)
+    return cfg
+
+
+def timed_repeats(region_ms: float) -> int:
+    """How many times to repeat a K-step timed region of about region_ms."""
+    return int(max(1, min(200, math.ceil(TIMED_TARGET_MS / max(region_ms, 1e-3)))))
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -242,9 +286,20 @@ def whole_job_tflops(flops_per_step: float, world: int, ms_per_step: float) -> f
 
 # --------------------------------------------------------------- CPU leg ----
 
-def oracle_sample(name, seconds_target=12.0, threads=0):
-    """Time the fp64 oracle on a seeded sample of output rows of the workload;
-    returns (TFLOP/s, cores, description)."""
+def host_threads() -> int:
+    """Threads for the CPU oracle: every core this process may run on (the
+    launcher's OMP_NUM_THREADS=1 for the GPU ranks does not apply to it)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_sample(name, seconds_target=12.0, threads=None):
+    """Time the fp64 oracle on a seeded sample of output rows of the workload
+    (all host cores unless `threads` is given); returns (TFLOP/s, cores,
+    description)."""
+    threads = host_threads() if threads is None else threads
     import numpy as np
     import oracle
     from sdpa_inputs import make_qkv
@@ -286,7 +341,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     import numpy as np  # noqa: F401
-    per_step_target = max(1.0, min(20.0, 90.0 / max(1, args.steps + args.warmup)))
+    per_step_target = min(args.cpu_seconds, max(1.0, min(20.0, 90.0 / max(1, args.steps + args.warmup))))
     values = []
     desc, cores = "", 0
     if name in BWD_WORKLOADS:
@@ -303,12 +358,14 @@ def run_reference(args, rank, world):
     ms = step_flops(name) / (value * 1e12) * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "ms_per_step_source": "extrapolated: the workload's FLOPs at the rate measured on a bounded row sample "
+                              "(the whole workload is not run)",
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
-        "config": {"workload": describe(name), "flops_per_step": step_flops(name),
-                   "note": "fp64 CPU oracle on the host cores; each step times a bounded row sample and "
-                           "ms_per_step is extrapolated to the whole workload"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "config": workload_config(name, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "cpu_model": cpu_model(),
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -380,16 +437,25 @@ def run_gpu(args, rank, world, local_rank):
         time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # timed region 1: the K steps back to back, as a caller issues them
-    barrier()
+    # timed region 1: the K steps back to back, as a caller issues them;
+    # repeated (each repeat exactly K steps) until ~TIMED_TARGET_MS have been
+    # timed, so the clock samples cover the kernel under load; the value is
+    # the median repeat, the slowest rank's
+    def region1():
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            launch(i)
+        end.record(stream)
+        barrier()
+        return start.elapsed_time(end)
+
     t_wall0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        launch(i)
-    end.record(stream)
-    barrier()
-    total_ms = start.elapsed_time(end)
-    total_ms = max_over_ranks(total_ms, world, dev)
+    region_ms = [region1()]
+    n_rep = int(max_over_ranks(timed_repeats(region_ms[0]), world, dev))
+    for _ in range(n_rep - 1):
+        region_ms.append(region1())
+    total_ms = max_over_ranks(statistics.median(region_ms), world, dev)
     ms_per_step = total_ms / args.steps
     # timed region 2: the same K steps, each bracketed by its own events on
     # the launching stream (the kernel's launch duration for the roofline)
@@ -508,9 +574,11 @@ def run_gpu(args, rank, world, local_rank):
     if dtype == "e4m3":
         peak = peaks["bf16_tflops"] * 2.0       # FP8 dense rate is twice bf16's (4.5 vs 2.25 PF nominal)
         peak_note = f"bf16 burst ({peak_src}) x 2 nominal FP8/bf16 ratio"
+        nominal_tensor = NOMINAL["fp8_tflops"]
     else:
         peak = peaks["bf16_tflops"]
         peak_note = f"bf16 burst ({peak_src})"
+        nominal_tensor = NOMINAL["bf16_tflops"]
     achieved_gbs = step_bytes(name) / (avg_kernel_ms * 1e-3) / 1e9
     # the bound is whichever roofline time is longer: FLOPs at the tensor peak
     # or algorithmic bytes at the HBM peak
@@ -519,11 +587,13 @@ def run_gpu(args, rank, world, local_rank):
     if t_hbm > t_tensor:
         roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": stored_traffic(name),
-                    "peak_source": f"HBM copy ({peak_src})", "achieved_tflops": achieved,
+                    "peak_source": f"HBM copy ({peak_src})", "nominal_peak": NOMINAL["hbm_gbs"],
+                    "frac_of_nominal": achieved_gbs / NOMINAL["hbm_gbs"], "achieved_tflops": achieved,
                     "tensor_peak_tflops": peak}
     else:
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": stored_traffic(name), "peak_source": peak_note,
+                    "nominal_peak": nominal_tensor, "frac_of_nominal": achieved / nominal_tensor,
                     "achieved_hbm_gbs": achieved_gbs, "hbm_peak_gbs": peaks["hbm_gbs"]}
     roofline.update({"kernel": "sdpa_fwd_kernel", "algorithmic_bytes_per_launch": step_bytes(name),
                      "roofline_time_ms": max(t_tensor, t_hbm) * 1e3,
@@ -532,31 +602,39 @@ def run_gpu(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded N(0,1), inputs resident in HBM)",
-        "config": {"workload": describe(name), "B": B, "Hq": Hq, "Hkv": Hkv, "Sq": Sq, "Skv": Skv, "D": D,
-                   "causal": causal, "flops_per_step": flops, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2 ({n_sets} rotating input sets of {step_bytes(name) / 1e6:.1f} MB, "
-                         f"{n_sets * step_bytes(name) / 1e6:.0f} MB in all)"},
+        "config": workload_config(name, world,
+                                  l2=f"inputs larger than L2 ({n_sets} rotating input sets of "
+                                     f"{step_bytes(name) / 1e6:.1f} MB, {n_sets * step_bytes(name) / 1e6:.0f} MB in all)",
+                                  timed_region=f"{len(region_ms)} repeats of the {args.steps} steps (median repeat; "
+                                               f"{sum(region_ms):.0f} ms timed in all)"),
         "roofline": roofline,
         "e2e": {"value": whole_job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
                 "pipelined": "H2D / kernel / D2H on three streams over two device buffer sets",
                 "serial_ms_per_step": e2e_serial_ms,
                 "serial_value": whole_job_tflops(flops, world, e2e_serial_ms)},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (len(region_ms) + 1) * args.steps,
         "graph": {"ms_per_launch": graph_ms, "launches": 3 * g_launches,
                   "note": "the same launches captured in one CUDA graph and replayed (no Python call per launch); "
                           "timed regions 1 (back to back, gives value) and 2 (per-launch events, gives the "
                           "roofline's launch duration) hold K launches each"},
         "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
     }
+    if line["clocks"] and line["clocks"].get("sm_mhz"):
+        # time x clock: the work in SM cycles per step, comparable across runs at different clocks
+        line["clocks"]["ms_x_mhz_per_step"] = ms_per_step * line["clocks"]["sm_mhz"]
     if not args.no_cpu_baseline:
         tf, cores, desc = oracle_sample(name, seconds_target=args.cpu_seconds)
-        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+        tf1, _, desc1 = oracle_sample("tiny-mha", seconds_target=2.0, threads=1)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "cpu_model": cpu_model(),
+                                "kind": "oracle", "sample": desc,
+                                "single_thread": {"workload": describe("tiny-mha"), "value": tf1, "unit": "TFLOP/s",
+                                                  "cores": 1, "sample": desc1}}
     print(json.dumps(line), flush=True)
     return 0
 
 
-def oracle_bwd_sample(name, threads=0):
+def oracle_bwd_sample(name, threads=None):
     """Time the fp64 backward oracle on a bounded sample of the workload:
     batch 0, every KV head (the oracle runs one thread per KV head), the
     first S positions, S a multiple of 256 chosen for about 7.5e9 FLOP per
@@ -564,6 +642,7 @@ def oracle_bwd_sample(name, threads=0):
     import oracle
     from sdpa_inputs import make_qkv
 
+    threads = host_threads() if threads is None else threads
     w = spec(name)
     per_s2 = 10.0 * w.Hq * w.D * (0.5 if w.causal else 1.0)
     target = 7.5e9 * min(w.Hkv, os.cpu_count() or 1)
@@ -649,14 +728,22 @@ def run_gpu_bwd(args, rank, world, local_rank):
     if sampler:
         time.sleep(0.3)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+
+    def region1():
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            launch(i)
+        end.record(stream)
+        barrier()
+        return start.elapsed_time(end)
+
     t_wall0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        launch(i)
-    end.record(stream)
-    barrier()
-    ms_per_step = max_over_ranks(start.elapsed_time(end), world, dev) / args.steps
+    region_ms = [region1()]
+    n_rep = int(max_over_ranks(timed_repeats(region_ms[0]), world, dev))
+    for _ in range(n_rep - 1):
+        region_ms.append(region1())
+    ms_per_step = max_over_ranks(statistics.median(region_ms), world, dev) / args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -700,30 +787,47 @@ def run_gpu_bwd(args, rank, world, local_rank):
     # FP8: twice the measured bf16 peak (the nominal dense FP8 / bf16 ratio)
     peak = peaks["bf16_tflops"] * (2 if fp8 else 1)
     peak_note = f"2 x bf16 burst ({peak_src}), the nominal FP8 / bf16 ratio" if fp8 else f"bf16 burst ({peak_src})"
+    nominal_tensor = NOMINAL["fp8_tflops" if fp8 else "bf16_tflops"]
     line = {
         "metric": METRIC, "value": whole_job_tflops(flops, world, ms_per_step), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e5m2 (fp32 accumulate)" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1), inputs resident in HBM)",
-        "config": {"workload": "backward pass, " + describe(name) + (" (E5M2 dO)" if fp8 else ""), "B": B, "Hq": Hq,
-                   "Hkv": Hkv, "Sq": S, "Skv": S,
-                   "D": D, "causal": causal, "flops_per_step": flops, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2 ({n_sets} rotating input sets of {step_bytes(name) / 1e6:.1f} MB)"},
+        "config": workload_config(name, world,
+                                  l2=f"inputs larger than L2 ({n_sets} rotating input sets of "
+                                     f"{step_bytes(name) / 1e6:.1f} MB)",
+                                  timed_region=f"{len(region_ms)} repeats of the {args.steps} steps (median repeat; "
+                                               f"{sum(region_ms):.0f} ms timed in all)"),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": stored_traffic(name), "peak_source": peak_note,
+                     "traffic": stored_traffic(name), "peak_source": peak_note, "nominal_peak": nominal_tensor,
+                     "frac_of_nominal": achieved / nominal_tensor,
                      "kernel": ("sdpa_bwd_fp8_kernel" if fp8 else "sdpa_bwd_kernel") + " (+ Delta, "
                      "dQ conversion; launch duration of the whole call)",
                      "algorithmic_bytes_per_launch": step_bytes(name)},
         "e2e": {"value": whole_job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms, "pipelined": "no (serial copy in, pass, copy out)"},
-        "gpu_launches": 2 * args.steps * 3,
+        "gpu_launches": (len(region_ms) + 1) * args.steps * 3,
         "clocks": sampler.summary(t_wall0, t_wall1) if sampler else None,
     }
+    if line["clocks"] and line["clocks"].get("sm_mhz"):
+        line["clocks"]["ms_x_mhz_per_step"] = ms_per_step * line["clocks"]["sm_mhz"]
     if not args.no_cpu_baseline and world == 1:
         tf, cores, desc = oracle_bwd_sample(name)
-        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "cpu_model": cpu_model(),
+                                "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def launch_command(n_gpus, argv):
+    """The torchrun command line that runs this script with `argv` as one
+    rank per GPU on this node (rendezvous on 127.0.0.1, a free port)."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n_gpus}",
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
 
 
 def main():
@@ -739,9 +843,17 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # one process per GPU: start this same command under torchrun
+        os.execv(sys.executable, launch_command(args.gpus, sys.argv[1:]))
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+        return 2
     if args.impl == "reference":
         return run_reference(args, rank, world)
     if world > 1:
