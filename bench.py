@@ -575,10 +575,12 @@ def run_gpu(args, rank, world, local_rank):
         peak = peaks["bf16_tflops"] * 2.0       # FP8 dense rate is twice bf16's (4.5 vs 2.25 PF nominal)
         peak_note = f"bf16 burst ({peak_src}) x 2 nominal FP8/bf16 ratio"
         nominal_tensor = NOMINAL["fp8_tflops"]
+        sustained = peaks["bf16_tflops_sustained"] * 2.0
     else:
         peak = peaks["bf16_tflops"]
         peak_note = f"bf16 burst ({peak_src})"
         nominal_tensor = NOMINAL["bf16_tflops"]
+        sustained = peaks["bf16_tflops_sustained"]
     achieved_gbs = step_bytes(name) / (avg_kernel_ms * 1e-3) / 1e9
     # the bound is whichever roofline time is longer: FLOPs at the tensor peak
     # or algorithmic bytes at the HBM peak
@@ -593,6 +595,7 @@ def run_gpu(args, rank, world, local_rank):
     else:
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": stored_traffic(name), "peak_source": peak_note,
+                    "sustained_peak": sustained, "frac_of_sustained": achieved / sustained,
                     "nominal_peak": nominal_tensor, "frac_of_nominal": achieved / nominal_tensor,
                     "achieved_hbm_gbs": achieved_gbs, "hbm_peak_gbs": peaks["hbm_gbs"]}
     roofline.update({"kernel": "sdpa_fwd_kernel", "algorithmic_bytes_per_launch": step_bytes(name),
@@ -788,6 +791,7 @@ def run_gpu_bwd(args, rank, world, local_rank):
     peak = peaks["bf16_tflops"] * (2 if fp8 else 1)
     peak_note = f"2 x bf16 burst ({peak_src}), the nominal FP8 / bf16 ratio" if fp8 else f"bf16 burst ({peak_src})"
     nominal_tensor = NOMINAL["fp8_tflops" if fp8 else "bf16_tflops"]
+    sustained = peaks["bf16_tflops_sustained"] * (2 if fp8 else 1)
     line = {
         "metric": METRIC, "value": whole_job_tflops(flops, world, ms_per_step), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -799,7 +803,8 @@ def run_gpu_bwd(args, rank, world, local_rank):
                                   timed_region=f"{len(region_ms)} repeats of the {args.steps} steps (median repeat; "
                                                f"{sum(region_ms):.0f} ms timed in all)"),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": stored_traffic(name), "peak_source": peak_note, "nominal_peak": nominal_tensor,
+                     "traffic": stored_traffic(name), "peak_source": peak_note, "sustained_peak": sustained,
+                     "frac_of_sustained": achieved / sustained, "nominal_peak": nominal_tensor,
                      "frac_of_nominal": achieved / nominal_tensor,
                      "kernel": ("sdpa_bwd_fp8_kernel" if fp8 else "sdpa_bwd_kernel") + " (+ Delta, "
                      "dQ conversion; launch duration of the whole call)",

@@ -994,4 +994,21 @@ int sdpa_abi_version(void)
     return 5;
 }
 
+#ifdef SDPA_WAIT_TEST
+// Test build only (not declared in include/sdpa.h, not in the product
+// library): sets the device wait limit in nanoseconds and the K-ring position
+// (per CTA, counted from 0) whose copy the forward producer leaves out (-1:
+// none).  With a position set, the waits that depend on that tile run out
+// after `limit_ns`, the kernel records its code in the device error word and
+// returns; the tests read the code through sdpa_device_error().
+sdpa_status_t sdpa_test_set_wait(unsigned long long limit_ns, int withhold_k)
+{
+    const uint64_t lim = limit_ns;
+    cudaError_t e = cudaMemcpyToSymbol(sdpa::g_test_wait_limit_ns, &lim, sizeof lim);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbol(sdpa::g_test_withhold_k, &withhold_k, sizeof withhold_k);
+    return e == cudaSuccess ? SDPA_OK : cuda_fail(e);
+}
+#endif
+
 }  // extern "C"

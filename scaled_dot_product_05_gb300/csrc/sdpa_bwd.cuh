@@ -268,8 +268,10 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                 c * kCe, h, qt * kBlockM, b);
                 ++issued;
             }
-            if (*abort) {
-                // never leave the CTA with copies in flight
+            {
+                // never leave the CTA with copies in flight: the last phase of
+                // every slot (complete already in a normal run; after an
+                // abort, the copies still landing)
                 drain_wait(smem_u32(&bars->kv_full), 0);
                 // issued counts the loads in order (Q of a tile, then its dO)
                 for (int k = (issued > 4 ? issued - 4 : 0); k < issued; ++k) {

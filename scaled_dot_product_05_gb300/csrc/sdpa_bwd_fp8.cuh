@@ -245,8 +245,10 @@ sdpa_bwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 tma_load_4d(sDO + s * L::kTileBytes, &tm_do, smem_u32(&bars->q_full[s]), 0, h, qt * kBlockM, b);
                 ++issued;
             }
-            if (*abort) {
-                // never leave the CTA with copies in flight
+            {
+                // never leave the CTA with copies in flight: the last phase of
+                // every slot (complete already in a normal run; after an
+                // abort, the copies still landing)
                 drain_wait(smem_u32(&bars->kv_full), 0);
                 for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it)
                     drain_wait(smem_u32(&bars->q_full[it & 1]), (it >> 1) & 1);

@@ -71,6 +71,18 @@ constexpr float kLn2 = 0.6931471805599453f;
 // CTA (see the codes below).  Read and cleared by the host through the C-ABI.
 __device__ unsigned int g_sdpa_error = 0;
 
+#ifdef SDPA_WAIT_TEST
+// Test build only (compiled with -DSDPA_WAIT_TEST into a separate library):
+// the wait limit and a K-ring position whose copy the forward producer leaves
+// out, both set from the host, so that a test can make a bounded wait run out
+// on the GPU without any fault.  The product library has neither.
+__device__ uint64_t g_test_wait_limit_ns = kWaitLimitNs;
+__device__ int g_test_withhold_k = -1;
+__device__ __forceinline__ uint64_t wait_limit_ns() { return g_test_wait_limit_ns; }
+#else
+__device__ __forceinline__ constexpr uint64_t wait_limit_ns() { return kWaitLimitNs; }
+#endif
+
 // Polls of the S-issue count before a P V MMA is issued anyway (~30 cycles
 // each): about twice the longest S_t(j+1) delay seen in clock traces.
 constexpr int kOrderSpins = 256;
@@ -189,7 +201,7 @@ struct Barriers {
     int abort;
 };
 
-// Bounded wait: gives up after kWaitLimitNs, records `code` in the device
+// Bounded wait: gives up after kWaitLimitNs (2 s), records `code` in the device
 // error word, and raises the CTA's abort flag so that every later wait in the
 // CTA returns at once.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int code)
@@ -202,7 +214,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
             return true;
         if (*abort)
             return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > wait_limit_ns()) {
             *abort = 1;
             atomicCAS(&g_sdpa_error, 0u, code);
             return false;
@@ -215,7 +227,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 {
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
+    while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < wait_limit_ns()) {
     }
 }
 
@@ -594,6 +606,12 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const uint32_t s = nk % NK;
                 if (nk >= NK && !wait_bar(smem_u32(&bars->k_empty[s]), ((nk / NK) & 1) ^ 1, abort, kErrWaitLoad + 3))
                     return false;
+#ifdef SDPA_WAIT_TEST
+                if ((int)nk == g_test_withhold_k) {        // test build: this K copy is never issued
+                    ++nk;
+                    return true;
+                }
+#endif
                 mbar_arrive_expect_tx(smem_u32(&bars->k_full[s]), L::kTileBytes);
                 for (int c = 0; c < L::kChunks; ++c)
                     tma_load_4d(sK + s * L::kTileBytes + c * L::kChunkBytes, &tm_k, smem_u32(&bars->k_full[s]),
@@ -624,8 +642,11 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int j = 1; ok && j < n; ++j)
                     ok = load_k(w, j) && load_v(w, j);
             }
-            if (*abort) {
-                // never leave the CTA with copies in flight
+            {
+                // never leave the CTA with copies in flight: wait (bounded)
+                // for the last use of every slot -- at once in a normal run,
+                // where the consumers have waited for them; after an abort,
+                // for the copies still landing
                 for (int t = 0; t < 2; ++t)
                     if (nq[t] > 0)
                         drain_wait(smem_u32(&bars->q_full[t]), (nq[t] - 1) & 1);
