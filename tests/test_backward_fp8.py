@@ -20,6 +20,15 @@ error is 2^-2(m+1) / 3 * 3 / (8 ln 2), a relative RMS of 2^-(m+1) / sqrt(8 ln 2)
     2^-30 amax stays in E5M2's normal range.  The test allows 0.08.
   * The rest (fp32 accumulation, exp2 of fp32 scores, bf16 O in Delta and the
     bf16 outputs, <= 2^-9 relative) is an order below.
+  * When O and the LSE come from the library's own FP8 forward, its E4M3
+    weights (relative RMS 0.027 each, independent, unbiased) move a row's LSE
+    (the log of their sum) and O (their weighted mean of V) by about
+    0.027 / sqrt(n_eff) relative, n_eff the row's effective number of keys;
+    the backward inherits shifts of that order (P = exp(S - LSE) scales by
+    exp(-dLSE), Delta = dO . O).  Only the first rows under the causal mask
+    have few keys, a negligible share of the tensor-wide RMS, so those tests
+    allow 0.01 more (measured 0.054 / 0.053 / 0.027 after the library's
+    forward, 0.053 / 0.053 / 0.025 after the oracle's).
 A mistake of layout, format or scale (a transposed operand, E4M3 read as
 E5M2, a descale dropped or applied twice) gives relative errors of order 1.
 The largest single error is also bounded by 0.25 of the tensor's largest
@@ -36,6 +45,8 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
 TOL = {"dQ": 0.08, "dK": 0.08, "dV": 0.04}
+# O and the LSE from the library's FP8 forward (its E4M3 weights): 0.01 more
+TOL_AFTER_FWD = {k: v + 0.01 for k, v in TOL.items()}
 MAX_FRAC = 0.25
 
 
@@ -125,8 +136,8 @@ def test_fp8_backward_gqa_1024():
 
 def test_fp8_backward_after_library_forward():
     # O and the LSE from sdpa_fwd_fp8_ex, as in training; the forward's own
-    # E4M3 rounding of P moves O by <= 6e-2 and the LSE by <= 8e-2 (its
-    # tolerances), which the gradients inherit: allow 0.05 more relative RMS
+    # E4M3 weights shift the gradients by ~0.027 / sqrt(n_eff) relative (see
+    # the module docstring): allow 0.01 more relative RMS
     from scaled_dot_product_05_gb300 import sdpa_fwd_fp8_ex
     shape, causal = (1, 4, 2, 384, 384, 128), True
     B, Hq, Hkv, Sq, Skv, D = shape
@@ -139,8 +150,7 @@ def test_fp8_backward_after_library_forward():
     amax = torch.zeros(1, dtype=torch.float32, device=DEV)
     run_kernel(x, g8, ddo, o, lse, causal, 1.0, amax)
     got = run_kernel(x, g8, ddo, o, lse, causal, E5M2_MAX / float(amax.item()))
-    check(got, reference(x, g8, ddo, causal), "after library forward",
-          tol={k: v + 0.05 for k, v in TOL.items()})
+    check(got, reference(x, g8, ddo, causal), "after library forward", tol=TOL_AFTER_FWD)
 
 
 def test_fp8_dk_dv_deterministic():
@@ -205,15 +215,14 @@ def test_fp8_backward_full_size_one_head():
     sl = lambda t: t[b:b + 1, :, h:h + 1].contiguous()
     q, k, v = (dequant(sl(t), d) for t, d in zip((x.q, x.k, x.v), (dq_, dk_, dv_)))
     ref = oracle.sdpa_backward_reference(q, k, v, dequant(sl(g8), ddo), causal=True, dtype="f64")
-    check([a[b:b + 1, :, h:h + 1] for a in got], ref, "full size, one head",
-          tol={k: v + 0.05 for k, v in TOL.items()})
+    check([a[b:b + 1, :, h:h + 1] for a in got], ref, "full size, one head", tol=TOL_AFTER_FWD)
 
 
 def library_fp8_forward(x):
     # O and the LSE for the full-size case come from the library's FP8
     # forward (the oracle's forward at this size would take minutes); its
-    # rounding of P moves them within the forward's tolerances, which the
-    # 0.05 margin of test_fp8_backward_after_library_forward covers
+    # weights shift the gradients by ~0.027 / sqrt(n_eff) relative, within
+    # the 0.01 margin of TOL_AFTER_FWD
     from scaled_dot_product_05_gb300 import sdpa_fwd_fp8_ex
     B, S, H, D = x.q.shape
     o = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=DEV)
