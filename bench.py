@@ -177,6 +177,12 @@ def workload_config(name, world, **extra):
     return cfg
 
 
+def queue_fill_cycles(steps: int) -> int:
+    """GPU clock cycles of sleep that cover the host's submission of `steps`
+    bracketed launches (~30 us each at ~2 GHz), at most ~20 ms."""
+    return int(min(4e7, 6e4 * steps))
+
+
 def timed_repeats(region_ms: float) -> int:
     """How many times to repeat a K-step timed region of about region_ms."""
     return int(max(1, min(200, math.ceil(TIMED_TARGET_MS / max(region_ms, 1e-3)))))
@@ -458,7 +464,10 @@ def run_gpu(args, rank, world, local_rank):
     total_ms = max_over_ranks(statistics.median(region_ms), world, dev)
     ms_per_step = total_ms / args.steps
     # timed region 2: the same K steps, each bracketed by its own events on
-    # the launching stream (the kernel's launch duration for the roofline)
+    # the launching stream (the kernel's launch duration for the roofline);
+    # they queue up behind a short GPU sleep, so that each pair of events
+    # brackets its kernel alone, without the host's submission gaps
+    torch.cuda._sleep(queue_fill_cycles(args.steps))
     for i in range(args.steps):
         ev[i][0].record(stream)
         launch(i)
@@ -748,6 +757,7 @@ def run_gpu_bwd(args, rank, world, local_rank):
         region_ms.append(region1())
     ms_per_step = max_over_ranks(statistics.median(region_ms), world, dev) / args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda._sleep(queue_fill_cycles(args.steps))     # the launches queue up behind it
     for i in range(args.steps):
         ev[i][0].record(stream)
         launch(i)
