@@ -17,11 +17,13 @@
 //                  each with its own full / empty barriers
 //   warp 1       tcgen05 issue, per query tile: S^T = K Q^T (cols 0..127;
 //                  at D = 64 alternately cols 384..511), dP^T = V dO^T
-//                  (cols 128..255); dV += P^T dO once P^T is packed, dK +=
-//                  dS^T Q once dS^T is (both read from TMEM); dQ_part = dS K
-//                  (dS from shared memory, an MN-major A operand) into cols
-//                  128..128+D-1.  The next tile's S^T goes in as early as its
-//                  columns and its Q allow
+//                  (cols 128..255); dV += P^T dO once P^T is packed (P^T read
+//                  from TMEM); once dS is in shared memory, dQ_part = dS K
+//                  (dS an MN-major A operand) into cols 128..128+D-1 first,
+//                  so that its read-out frees them for the next dP^T, then
+//                  dK += dS^T Q (the same tile as a K-major A operand).  The
+//                  next tile's S^T goes in as early as its columns and its Q
+//                  allow
 //   warp 2       dQ reducer: adds the staged dQ_part of a query tile into
 //                  the fp32 dQ accumulator in HBM (TMA bulk reductions), then
 //                  hands the tile's Q, then dO, back to the producer
@@ -29,15 +31,16 @@
 //                  into a double-buffered shared array
 //   warps 4..11  two warpgroups, one thread per key row each, the first for
 //                  queries 0..63 of the tile, the second for 64..127: first
-//                  P^T = exp2(S^T c - LSE2) (from S^T alone), then dS^T =
-//                  scale P^T (dP^T - Delta), each written as 16-bit values
-//                  over S^T / dP^T in TMEM, dS^T also to shared memory for
-//                  dQ; at the end dV (first) and dK (second) to HBM
-//   warps 12..15 one thread per query row: dQ_part from TMEM, staged in
-//                  shared memory over the tile's Q and dO (every MMA that
-//                  reads them precedes the dQ MMA; 128 x D fp32 is exactly
-//                  their size), for the reducer (every key tile of a query
-//                  row contributes to its dQ)
+//                  P^T = exp2(S^T c - LSE2) (from S^T alone), packed as
+//                  16-bit values over S^T in TMEM, then dS^T = scale P^T
+//                  (dP^T - Delta) into a 16-bit shared tile for the dQ and dK
+//                  MMAs; at the end dV (first) and dK (second) to HBM
+//   warps 12..15 one thread per query row: dQ_part from TMEM (freeing its
+//                  columns), then, once the tile's dK MMA (the last reader of
+//                  its Q and dO) is done, staged in shared memory over the
+//                  tile's Q and dO (128 x D fp32 is exactly their size), for
+//                  the reducer (every key tile of a query row contributes to
+//                  its dQ)
 // A preprocessing kernel forms Delta, a final one converts the fp32 dQ
 // (both in sdpa_bwd_prep.cuh).
 #pragma once
@@ -97,8 +100,9 @@ struct BwdBarriers {
     uint64_t dp_full;                // dP^T in TMEM
     uint64_t p_ready;                // P^T packed in TMEM (both softmax warpgroups)
     uint64_t ds_ready;               // dS^T packed in TMEM and shared memory
-    uint64_t dq_full;
-    uint64_t dq_free;
+    uint64_t dq_full;                // dQ_part of the tile in TMEM
+    uint64_t dq_free;                // dQ_part read out of TMEM (its columns free for the next dP^T)
+    uint64_t dk_done;                // the tile's dK MMA complete (its Q / dO stage may take dQ_part)
     uint64_t dkv_full;
     uint64_t stats_full[2];          // LSE2 / Delta buffer written (count 32)
     uint64_t dstage_full[2][4];      // dQ_part slice j staged over Q / dO stage s (count 128)
@@ -208,6 +212,7 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_init(smem_u32(&bars->ds_ready), 256);
         mbar_init(smem_u32(&bars->dq_full), 1);
         mbar_init(smem_u32(&bars->dq_free), 128);
+        mbar_init(smem_u32(&bars->dk_done), 1);
         mbar_init(smem_u32(&bars->dkv_full), 1);
         mbar_init(smem_u32(&bars->stats_full[0]), 32);
         mbar_init(smem_u32(&bars->stats_full[1]), 32);
@@ -295,7 +300,8 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t mnmaj = (uint32_t)(L::kChunkBytes >> 4) << 16;
             const uint32_t k_lo = (sK >> 4) | kmaj, k_mn = (sK >> 4) | mnmaj;
             const uint32_t v_lo = (sV >> 4) | kmaj;
-            const uint32_t ds_lo = (sDS >> 4) | ((uint32_t)(L::kDSChunkBytes >> 4) << 16);
+            const uint32_t ds_lo = (sDS >> 4) | ((uint32_t)(L::kDSChunkBytes >> 4) << 16);   // MN-major use
+            const uint32_t dsk_lo = (sDS >> 4) | kmaj;                                          // K-major use
             const uint32_t dp_t = tmem + L::kColDP;
             auto s_of = [&](int it) -> uint32_t { return tmem + ((L::kTwoS && (it & 1)) ? L::kColS2 : L::kColS); };
             const uint32_t dv_t = tmem + L::kColDV, dk_t = tmem + L::kColDK;
@@ -367,27 +373,30 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         break;
                     s_next = true;
                 }
-                // dK += dS^T Q, dS^T from TMEM like P^T; Q MN-major
+                // dQ_part = dS K first, into cols 128..128+D-1 (free once the
+                // softmax has read dP^T): its read-out frees those columns for
+                // the next dP^T.  A = dS (queries x keys) from the dS^T tile read
+                // MN-major, 16 keys (rows of 128 bytes) per step; K MN-major.
                 if (!(ok = wait_bar(smem_u32(&bars->ds_ready), it & 1, abort, kErrBwdWait + 10)))
                     break;
                 tc_fence_after_sync();
-#pragma unroll
-                for (int kk = 0; kk < kBlockM / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk * 16 * L::kSwz) >> 4);
-                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-                    const uint32_t col = (kk < 4) ? 8 * kk : 32 + 8 * kk;
-                    mma_f16_ts(dk_t, dp_t + col, desc_join(hi, q_mn + off), id_o, acc);
-                }
-                // dQ_part = dS K: A = dS (queries x keys) from the dS^T tile read
-                // MN-major, 16 keys (rows of 128 bytes) per step; K MN-major.
-                // Into cols 128..128+D-1: issued after the dK MMA read dS^T there.
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk) {
                     const uint32_t off_a = (uint32_t)((kk * 16 * 128) >> 4);
                     const uint32_t off_b = (uint32_t)((kk * 16 * L::kSwz) >> 4);
                     mma_f16_ss(dp_t, desc_join(hi_ds, ds_lo + off_a), desc_join(hi, k_mn + off_b), id_q, kk > 0);
                 }
-                mma_commit(smem_u32(&bars->dq_full));       // also frees Q / dO stage s for dQ staging
+                mma_commit(smem_u32(&bars->dq_full));
+                // dK += dS^T Q: A = the same dS^T tile read K-major (key rows,
+                // 16 queries = 32 bytes per step, 64-query chunks), Q MN-major
+#pragma unroll
+                for (int kk = 0; kk < kBlockM / 16; ++kk) {
+                    const uint32_t off_a = (uint32_t)(((kk / 4) * L::kDSChunkBytes + (kk % 4) * 32) >> 4);
+                    const uint32_t off_b = (uint32_t)((kk * 16 * L::kSwz) >> 4);
+                    const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+                    mma_f16_ss(dk_t, desc_join(hi_ds, dsk_lo + off_a), desc_join(hi, q_mn + off_b), id_o, acc);
+                }
+                mma_commit(smem_u32(&bars->dk_done));       // Q / dO of stage s: no MMA reads them any more
                 if (!s_next && !(ok = issue_s(it + 1)))
                     break;
             }
@@ -531,8 +540,7 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     dk[2 * i] = pack2<kOutBF16>(ds[0], ds[1]);
                     dk[2 * i + 1] = pack2<kOutBF16>(ds[2], ds[3]);
                 }
-                tmem_st16(dp_t + 64 * sw + 16 * chh, dk);
-                // dS^T row for dQ: queries 32ch .. 32ch+31 are 16-byte units
+                // dS^T row for the dQ and dK MMAs: queries 32ch .. 32ch+31 are 16-byte units
                 // 4(ch&1) .. +3 of 64-query chunk ch/2 (= sw), 128-byte swizzle
                 const uint32_t row_base = sDS + sw * L::kDSChunkBytes + kr * 128;
 #pragma unroll
@@ -543,7 +551,6 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             }
             fence_proxy_async_smem();
-            tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(smem_u32(&bars->ds_ready));
         }
@@ -602,10 +609,13 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld32_wait(src + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
             tc_fence_before_sync();
             mbar_arrive(smem_u32(&bars->dq_free));
-            // staged for the reducer over Q / dO stage s (free: every MMA of
-            // the tile has completed): 32-column slices of 128 rows x 128
-            // bytes with the 128-byte swizzle, slices 0 .. D/64-1 over Q and
-            // the rest over dO
+            // staged for the reducer over Q / dO stage s once the tile's dK
+            // MMA, their last reader, has completed: 32-column slices of 128
+            // rows x 128 bytes with the 128-byte swizzle, slices 0 .. D/64-1
+            // over Q and the rest over dO
+            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->dk_done), it & 1, abort, kErrBwdWait + 17));
+            if (!ok)
+                break;
             const int s = it & 1;
 #pragma unroll
             for (int j = 0; j < D / 32; ++j) {

@@ -319,27 +319,28 @@ sdpa_bwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         break;
                     s_next = true;
                 }
-                // dK += dS8^T Q: dS8^T K-major, Q MN-major
+                // dQ_part = dS8 K first, into cols 128..128+D-1 (free once the
+                // softmax has read dP^T), so that its read-out frees them for
+                // the next dP^T: A = the dS8^T tile read MN-major (32 key rows
+                // per step), K MN-major (32 key rows per step)
                 if (!(ok = wait_bar(smem_u32(&bars->ds_ready), it & 1, abort, kErrBwd8Wait + 6)))
                     break;
                 tc_fence_after_sync();
-#pragma unroll
-                for (int kk = 0; kk < kBlockM / 32; ++kk) {
-                    const uint32_t off = (uint32_t)((kk * 32 * L::kRowBytes) >> 4);
-                    mma_f8_ss(dk_t, desc_join(hi_t, ds_lo + 2 * kk), desc_join(hi, q_lo + off), id_dk,
-                              (it > 0 || kk > 0) ? 1u : 0u);
-                }
-                // dQ_part = dS8 K into cols 128..128+D-1 (after the dK MMA, in
-                // order): A = the dS8^T tile read MN-major (32 key rows per
-                // step), K MN-major (32 key rows per step)
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 32; ++kk) {
                     const uint32_t off_a = (uint32_t)((kk * 32 * 128) >> 4);
                     const uint32_t off_b = (uint32_t)((kk * 32 * L::kRowBytes) >> 4);
                     mma_f8_ss(dp_t, desc_join(hi_t, ds_lo + off_a), desc_join(hi, k_lo + off_b), id_dq, kk > 0);
                 }
-                mma_commit(smem_u32(&bars->q_empty[s]));
                 mma_commit(smem_u32(&bars->dq_full));
+                // dK += dS8^T Q: dS8^T K-major, Q MN-major
+#pragma unroll
+                for (int kk = 0; kk < kBlockM / 32; ++kk) {
+                    const uint32_t off = (uint32_t)((kk * 32 * L::kRowBytes) >> 4);
+                    mma_f8_ss(dk_t, desc_join(hi_t, ds_lo + 2 * kk), desc_join(hi, q_lo + off), id_dk,
+                              (it > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&bars->q_empty[s]));     // the dK MMA was Q's last reader
                 if (!s_next && !(ok = issue_s(it + 1)))
                     break;
             }
