@@ -218,8 +218,15 @@ sdpa_bwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
-    auto head_of = [&](int it) { return hkv * p.group + it / n_q; };
-    auto qtile_of = [&](int it) { return qt0 + it % n_q; };
+    // (head, query tile) of iteration it: head-major with ascending query
+    // tiles; for causal passes with 8 or more query heads per KV head, query
+    // tiles from the last down with the heads innermost, so that the CTAs of
+    // a KV head work on the same few query tiles at a time (measured on one
+    // box: causal MQA S=4096 846 against 785 TFLOP/s; non-causal MQA 958
+    // against 1030 and GQA with 4 heads -2 %, which keep the first order)
+    const bool heads_inner = p.causal && p.group >= 8;
+    auto head_of = [&](int it) { return hkv * p.group + (heads_inner ? it % p.group : it / n_q); };
+    auto qtile_of = [&](int it) { return heads_inner ? p.n_qt - 1 - it / p.group : qt0 + it % n_q; };
 
     if (warp < kSoftmaxWarp0) {
       regs_release<kRegsLow>();

@@ -69,6 +69,7 @@ SHAPES = [
     (1, 8, 1, 200, 77, 64),
     (1, 4, 4, 77, 333, 128),
     (2, 2, 2, 513, 513, 128),
+    (1, 16, 2, 384, 384, 128),     # 8 query heads per KV head: query tiles last-first, heads innermost
 ]
 
 
