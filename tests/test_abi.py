@@ -1,6 +1,12 @@
 """C ABI checks that need no GPU: the library builds and loads, exports every
 function include/sdpa.h declares, and rejects bad arguments with the
-documented status before any CUDA call."""
+documented status before any CUDA call.
+
+The argument checks pass fake device addresses that nothing may dereference.
+Where a CUDA device can be reached, a call whose arguments got past every
+check (the contiguous-layout case below, or a check that regressed) would
+launch a kernel on those addresses, so every such test skips there: they are
+CPU-only by construction, not just by their marker."""
 import ctypes
 import math
 import os
@@ -19,6 +25,15 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def lib():
     cuda_build.build()
     return _abi.lib()
+
+
+@pytest.fixture
+def fake(lib):
+    """The library, for calls that pass fake device addresses: only where no
+    GPU can be reached."""
+    if torch.cuda.is_available():
+        pytest.skip("fake device addresses are passed only where no GPU can be reached")
+    return lib
 
 
 def declared_functions():
@@ -69,12 +84,12 @@ def call(lib, q=QP, k=KP, v=VP, o=OP, **kw):
     (dict(scale=0.0), 7), (dict(scale=-1.0), 7), (dict(scale=float("inf")), 7), (dict(scale=float("nan")), 7),
     (dict(o=QP + 16), 9), (dict(o=VP - 64), 9),
 ])
-def test_rejects_before_any_cuda_call(lib, kw, status):
-    assert call(lib, **kw) == status
+def test_rejects_before_any_cuda_call(fake, kw, status):
+    assert call(fake, **kw) == status
 
 
-def test_fp8_entry_checks(lib):
-    f = lib.sdpa_fwd_fp8
+def test_fp8_entry_checks(fake):
+    f = fake.sdpa_fwd_fp8
     s = ctypes.c_float
     assert f(QP, KP, VP, None, 1, 2, 2, 128, 128, 64, s(0.125), s(1), s(1), s(1), 0, None) == 1
     assert f(QP, KP, VP, OP, 1, 2, 2, 128, 128, 64, s(0.125), s(0.0), s(1), s(1), 0, None) == 7
@@ -83,11 +98,10 @@ def test_fp8_entry_checks(lib):
     assert f(QP, KP, VP, OP, 1, 2, 2, 128, 128, 48, s(0.125), s(1), s(1), s(1), 0, None) == 5
 
 
-@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
-def test_valid_call_without_gpu_reports_cuda_error(lib):
-    st = call(lib)
+def test_valid_call_without_gpu_reports_cuda_error(fake):
+    st = call(fake)
     assert st == 10
-    assert lib.sdpa_last_cuda_error() != 0
+    assert fake.sdpa_last_cuda_error() != 0
 
 
 def test_binding_rejects_cpu_tensors():
@@ -126,21 +140,21 @@ BHSD_Q = (HQ * SQ * D_, D_, SQ * D_)
     (dict(dtype=2), 6),
     (dict(q=None), 1),
 ])
-def test_ex_rejects_before_any_cuda_call(lib, kw, status):
-    assert call_ex(lib, **kw) == status
+def test_ex_rejects_before_any_cuda_call(fake, kw, status):
+    assert call_ex(fake, **kw) == status
 
 
-def test_ex_contiguous_layout_is_the_default(lib):
+def test_ex_contiguous_layout_is_the_default(fake):
     # explicit contiguous strides pass the same checks as NULL layouts: the
     # only failure left is the device (none here) or a CUDA error
-    st_null = call_ex(lib)
-    st_expl = call_ex(lib, ql=BSHD_Q, kl=(SQ * HKV * D_, HKV * D_, D_), vl=(SQ * HKV * D_, HKV * D_, D_),
+    st_null = call_ex(fake)
+    st_expl = call_ex(fake, ql=BSHD_Q, kl=(SQ * HKV * D_, HKV * D_, D_), vl=(SQ * HKV * D_, HKV * D_, D_),
                       ol=BSHD_Q)
     assert st_null == st_expl and st_null in (8, 10)
 
 
-def test_fp8_ex_checks(lib):
-    f = lib.sdpa_fwd_fp8_ex
+def test_fp8_ex_checks(fake):
+    f = fake.sdpa_fwd_fp8_ex
     s = ctypes.c_float
     bad = ctypes.byref(_abi.Layout(128 * 2 * 64, 2 * 64, 8))    # 8-byte head stride
     assert f(QP, KP, VP, OP, None, 1, 2, 2, 128, 128, 64, bad, None, None, None,
@@ -162,8 +176,8 @@ def call_decode(lib, ws=None, ws_bytes=0, **kw):
     (dict(ws=0x50000008, ws_bytes=1 << 20), 12),   # workspace not 16-byte aligned
     (dict(D=48), 5),
 ])
-def test_decode_rejects_before_any_cuda_call(lib, kw, status):
-    assert call_decode(lib, **kw) == status
+def test_decode_rejects_before_any_cuda_call(fake, kw, status):
+    assert call_decode(fake, **kw) == status
 
 
 def test_decode_workspace_query_rejects_bad_sizes(lib):
@@ -172,9 +186,9 @@ def test_decode_workspace_query_rejects_bad_sizes(lib):
     assert lib.sdpa_decode_workspace_bytes(1, 8, 2, 1, 1000, 96) == 0
 
 
-def test_decode_noalloc_rejects_before_any_cuda_call(lib):
+def test_decode_noalloc_rejects_before_any_cuda_call(fake):
     s = ctypes.c_float
-    f = lib.sdpa_fwd_decode_noalloc
+    f = fake.sdpa_fwd_decode_noalloc
     assert f(QP, KP, VP, OP, None, 1, 12, 4, 1, 1000, 128, None, None, None, None, s(0.1), 0, None) == 4
     assert f(None, KP, VP, OP, None, 1, 8, 2, 1, 1000, 128, None, None, None, None, s(0.1), 0, None) == 1
     assert f(QP, KP, VP, OP, None, 1, 8, 2, 1, 1000, 128, None, None, None, None, s(0.1), 2, None) == 6
@@ -215,8 +229,8 @@ def call_bwd_fp8(lib, ws_bytes=None, descales=(0.01, 0.01, 0.01, 1e-3), scale_ds
     (dict(scale=0.0), 7), (dict(ws_bytes=1024), 12),
     (dict(dq=BP["q"] + 16), 9), (dict(dk=BP["ws"] + 64), 9), (dict(dv=BP["dk"]), 9),
 ])
-def test_bwd_rejects_before_any_cuda_call(lib, kw, status):
-    assert call_bwd(lib, **kw) == status
+def test_bwd_rejects_before_any_cuda_call(fake, kw, status):
+    assert call_bwd(fake, **kw) == status
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -228,8 +242,8 @@ def test_bwd_rejects_before_any_cuda_call(lib, kw, status):
     (dict(ws_bytes=4096), 12),
     (dict(dq=BP["q"] + 16), 9), (dict(amax=BP["ws"] + 64), 9), (dict(dk=BP["dv"]), 9),
 ])
-def test_bwd_fp8_rejects_before_any_cuda_call(lib, kw, status):
-    assert call_bwd_fp8(lib, **kw) == status
+def test_bwd_fp8_rejects_before_any_cuda_call(fake, kw, status):
+    assert call_bwd_fp8(fake, **kw) == status
 
 
 def test_bwd_fp8_workspace_bytes():
