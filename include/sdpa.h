@@ -240,7 +240,9 @@ size_t sdpa_bwd_workspace_bytes(int B, int Hq, int Sq, int D);
  * FP8 backward pass (section 10 of the codelab, "FP8": E4M3 tensors in the
  * forward pass, E5M2 for the backward pass), contiguous BSHD, D 64 or 128:
  * the gradients of sum(dO * O) for O = sdpa_fwd_fp8(Q, K, V), every GEMM on
- * the FP8 tensor cores with fp32 accumulation.
+ * the FP8 tensor cores with fp32 accumulation; dQ sums its per-key-tile parts
+ * in a bf16 accumulator (in the workspace), whose rounding is far below that
+ * of the E5M2 dS it multiplies.
  *   Q8, K8, V8  E4M3 codes (one byte each) of the forward's inputs, value =
  *               code * descale_q / descale_k / descale_v.
  *   O           the forward's bf16 output; LSE its log-sum-exp (fp32
@@ -254,8 +256,9 @@ size_t sdpa_bwd_workspace_bytes(int B, int Hq, int Sq, int D);
  *   amax_ds     device float, written: max |dS| of this call (before
  *               scaling), for the next call's scale_ds; NULL: not reported.
  *   workspace   device scratch of at least sdpa_bwd_fp8_workspace_bytes(B,
- *               Hq, Sq, D) bytes, 16-byte aligned, needing no
- *               initialisation, not used by a concurrent call.
+ *               Hq, Sq, D) bytes (B*Sq*Hq*D*2 + B*Hq*Sq*4 + 16), 16-byte
+ *               aligned, needing no initialisation, not used by a
+ *               concurrent call.
  * Descales and scale_ds must be finite and > 0 (else SDPA_ERR_SCALE).
  * Written buffers must not overlap one another or any input.  Other
  * arguments and statuses as for sdpa_bwd.

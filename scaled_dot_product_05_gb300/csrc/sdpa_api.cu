@@ -702,11 +702,17 @@ sdpa_status_t run_bwd(const void* Q, const void* K, const void* V, const void* O
     return SDPA_OK;
 }
 
-// FP8 backward workspace: the fp32 dQ accumulator and Delta as for the
-// 16-bit pass, then one 16-byte word for amax|dS| when the caller passes none.
+// FP8 backward workspace: the bf16 dQ accumulator [B][Sq][Hq][D], Delta
+// [B][Hq][Sq] (fp32), then one 16-byte word for amax|dS| when the caller
+// passes none.
+size_t bwd8_dq_bytes(int B, int Hq, int Sq, int D)
+{
+    return static_cast<size_t>(B) * Sq * Hq * D * 2;
+}
+
 size_t bwd8_workspace(int B, int Hq, int Sq, int D)
 {
-    return bwd_workspace(B, Hq, Sq, D) + 16;
+    return bwd8_dq_bytes(B, Hq, Sq, D) + static_cast<size_t>(B) * Hq * Sq * sizeof(float) + 16;
 }
 
 template <int D>
@@ -715,7 +721,7 @@ cudaError_t launch_bwd8(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
                         float dq_factor, cudaStream_t stream)
 {
     const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
-    cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(float), stream);
+    cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(uint16_t), stream);
     if (e != cudaSuccess || (e = cudaMemsetAsync(p.amax_ds, 0, sizeof(unsigned int), stream)) != cudaSuccess)
         return e;
     constexpr int kRows = 256 / (D / 16);
@@ -729,7 +735,7 @@ cudaError_t launch_bwd8(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
     const long long n = rows * D;
-    sdpa::bwd8::bwd8_dq_convert_kernel<<<static_cast<unsigned>((n / 4 + 255) / 256), 256, 0, stream>>>(
+    sdpa::bwd8::bwd8_dq_convert_kernel<<<static_cast<unsigned>((n / 8 + 255) / 256), 256, 0, stream>>>(
         p.dq_acc, dQ, n, dq_factor);
     return cudaGetLastError();
 }
@@ -774,21 +780,22 @@ sdpa_status_t run_bwd_fp8(const void* Q8, const void* K8, const void* V8, const 
     st = device_ready(&dev, &sm_count);
     if (st != SDPA_OK)
         return st;
-    float* dq_acc = static_cast<float*>(ws);
+    uint16_t* dq_acc = static_cast<uint16_t*>(ws);
     CUtensorMap tq, tk, tv, tdo, tdq;
     const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
     if (!make_map(&tq, Q8, u8, 1, s.D, s.Hq, s.Sq, s.B, fwd.q) || !make_map(&tk, K8, u8, 1, s.D, s.Hkv, s.Skv, s.B, fwd.k) ||
         !make_map(&tv, V8, u8, 1, s.D, s.Hkv, s.Skv, s.B, fwd.v) ||
         !make_map(&tdo, dO8, u8, 1, s.D, s.Hq, s.Sq, s.B, fwd.q) ||
-        !make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, s.D, s.Hq, s.Sq, s.B, fwd.q))
+        !make_map(&tdq, dq_acc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s.D, s.Hq, s.Sq, s.B, fwd.q))
         return cuda_fail(cudaErrorInvalidValue);
 
     sdpa::bwd8::Params p{};
     p.lse = LSE;
     p.dq_acc = dq_acc;
-    p.delta = dq_acc + static_cast<long long>(s.B) * s.Sq * s.Hq * s.D;
+    p.delta = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + bwd8_dq_bytes(s.B, s.Hq, s.Sq, s.D));
     p.amax_ds = amax_ds ? reinterpret_cast<unsigned int*>(amax_ds)
-                        : reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + bwd_workspace(s.B, s.Hq, s.Sq, s.D));
+                        : reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + bwd8_workspace(s.B, s.Hq, s.Sq, s.D) -
+                                                          16);
     p.dK = dK;
     p.dV = dV;
     p.B = s.B;

@@ -248,5 +248,7 @@ def test_bwd_fp8_rejects_before_any_cuda_call(fake, kw, status):
 
 def test_bwd_fp8_workspace_bytes():
     from scaled_dot_product_05_gb300 import bwd_fp8_workspace_bytes, bwd_workspace_bytes
-    assert bwd_fp8_workspace_bytes(2, 32, 4096, 128) == bwd_workspace_bytes(2, 32, 4096, 128) + 16
+    # the bf16 dQ accumulator, fp32 Delta per query row and head, one 16-byte amax word
+    assert bwd_fp8_workspace_bytes(2, 32, 4096, 128) == 2 * 4096 * 32 * 128 * 2 + 2 * 32 * 4096 * 4 + 16
+    assert bwd_fp8_workspace_bytes(2, 32, 4096, 128) < bwd_workspace_bytes(2, 32, 4096, 128)
     assert bwd_fp8_workspace_bytes(2, 32, 4096, 32) == 0
