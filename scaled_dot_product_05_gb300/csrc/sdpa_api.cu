@@ -601,14 +601,13 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 {
     constexpr bool kBF16 = (KIND == sdpa::kBF16);
     const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
-    cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(float), stream);
-    if (e != cudaSuccess)
-        return e;
+    // Delta, and the dQ accumulator zeroed, in one pass
     constexpr int kRows = sdpa::bwd::delta_rows_per_block<D>();
     sdpa::bwd::bwd_delta_kernel<D, kBF16>
         <<<static_cast<unsigned>((rows + kRows - 1) / kRows), sdpa::bwd::kDeltaThreads, 0, stream>>>(
-            O, dO, const_cast<float*>(p.delta), p.B, p.Hq, p.Sq);
-    if ((e = cudaGetLastError()) != cudaSuccess)
+            O, dO, const_cast<float*>(p.delta), p.dq_acc, p.B, p.Hq, p.Sq);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
         return e;
     const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.n_kt);
     sdpa::bwd::sdpa_bwd_kernel<D, KIND>
@@ -616,7 +615,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
     const long long n = rows * D;
-    sdpa::bwd::bwd_dq_convert_kernel<kBF16><<<static_cast<unsigned>((n / 4 + 255) / 256), 256, 0, stream>>>(
+    sdpa::bwd::bwd_dq_convert_kernel<kBF16><<<static_cast<unsigned>((n / 8 + 255) / 256), 256, 0, stream>>>(
         p.dq_acc, dQ, n);
     return cudaGetLastError();
 }
@@ -721,13 +720,13 @@ cudaError_t launch_bwd8(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
                         float dq_factor, cudaStream_t stream)
 {
     const long long rows = static_cast<long long>(p.B) * p.Hq * p.Sq;
-    cudaError_t e = cudaMemsetAsync(p.dq_acc, 0, static_cast<size_t>(rows) * D * sizeof(uint16_t), stream);
-    if (e != cudaSuccess || (e = cudaMemsetAsync(p.amax_ds, 0, sizeof(unsigned int), stream)) != cudaSuccess)
-        return e;
-    constexpr int kRows = 256 / (D / 16);
+    // Delta, the dQ accumulator and amax zeroed, in one pass (two rows per
+    // group of D / 16 lanes)
+    constexpr int kRows = 2 * (256 / (D / 16));
     sdpa::bwd8::bwd8_delta_kernel<D, true><<<static_cast<unsigned>((rows + kRows - 1) / kRows), 256, 0, stream>>>(
-        O, dO8, const_cast<float*>(p.delta), p.B, p.Hq, p.Sq);
-    if ((e = cudaGetLastError()) != cudaSuccess)
+        O, dO8, const_cast<float*>(p.delta), p.dq_acc, p.amax_ds, p.B, p.Hq, p.Sq);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
         return e;
     const unsigned grid = static_cast<unsigned>(static_cast<long long>(p.B) * p.Hkv * p.n_kt);
     sdpa::bwd8::sdpa_bwd_fp8_kernel<D>

@@ -593,44 +593,64 @@ sdpa_bwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
 // Delta8_i = sum_d dO8_id O_id (fp32): dO as E5M2 codes (one byte each), O
 // 16-bit, both [B][Sq][Hq][D]; written to the [B][Hq][Sq] layout.  One
-// group of D / 16 lanes per row, 16 codes (16 bytes) a lane.
+// group of D / 16 lanes per row, 16 codes (16 bytes) a lane, two rows a
+// group.  The same pass zeroes the row's D bf16 of the dQ accumulator
+// ([B][Sq][Hq][D]) and the amax word: one launch instead of two memsets and
+// this kernel.
 template <int D, bool kBF16>
-__global__ void __launch_bounds__(256) bwd8_delta_kernel(const void* O, const void* dO8, float* delta, int B,
-                                                         int Hq, int Sq)
+__global__ void __launch_bounds__(256) bwd8_delta_kernel(const void* O, const void* dO8, float* delta,
+                                                         uint16_t* dq_acc, unsigned int* amax, int B, int Hq, int Sq)
 {
     constexpr int kLanes = D / 16;
+    constexpr int kGroups = 256 / kLanes;
     const int64_t rows = (int64_t)B * Sq * Hq;
-    const int64_t row = (int64_t)blockIdx.x * (256 / kLanes) + threadIdx.x / kLanes;
     const int c = threadIdx.x % kLanes;
-    float acc = 0.f;
-    if (row < rows) {
-        const uint4 g = reinterpret_cast<const uint4*>(dO8)[row * kLanes + c];
-        const uint4* o = reinterpret_cast<const uint4*>(O) + (row * kLanes + c) * 2;
-        const uint4 o0 = o[0], o1 = o[1];
-        const uint32_t gv[4] = {g.x, g.y, g.z, g.w};
-        const uint32_t ov[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *amax = 0u;                                     // the main kernel's atomic max starts from 0
+    int64_t row[2];
+    uint4 g[2], o0[2], o1[2];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t g2 = e5m2x2_to_f16x2((uint16_t)(gv[k / 2] >> (16 * (k & 1))));
-            const float2 gf = __half22float2(*reinterpret_cast<const __half2*>(&g2));
-            float2 of;
-            if constexpr (kBF16)
-                of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[k]));
-            else
-                of = __half22float2(*reinterpret_cast<const __half2*>(&ov[k]));
-            acc = fmaf(gf.x, of.x, acc);
-            acc = fmaf(gf.y, of.y, acc);
+    for (int k = 0; k < 2; ++k) {
+        row[k] = (int64_t)blockIdx.x * (2 * kGroups) + k * kGroups + threadIdx.x / kLanes;
+        if (row[k] < rows) {
+            g[k] = reinterpret_cast<const uint4*>(dO8)[row[k] * kLanes + c];
+            const uint4* o = reinterpret_cast<const uint4*>(O) + (row[k] * kLanes + c) * 2;
+            o0[k] = o[0];
+            o1[k] = o[1];
         }
     }
 #pragma unroll
-    for (int s = kLanes / 2; s > 0; s >>= 1)
-        acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (row < rows && c == 0) {
-        const int hq = (int)(row % Hq);
-        const int64_t bi = row / Hq;
-        const int i = (int)(bi % Sq);
-        const int b = (int)(bi / Sq);
-        delta[((int64_t)b * Hq + hq) * Sq + i] = acc;
+    for (int k = 0; k < 2; ++k) {
+        float acc = 0.f;
+        if (row[k] < rows) {
+            uint4* z = reinterpret_cast<uint4*>(dq_acc + row[k] * D + 16 * c);
+            z[0] = make_uint4(0u, 0u, 0u, 0u);
+            z[1] = make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t gv[4] = {g[k].x, g[k].y, g[k].z, g[k].w};
+            const uint32_t ov[8] = {o0[k].x, o0[k].y, o0[k].z, o0[k].w, o1[k].x, o1[k].y, o1[k].z, o1[k].w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t g2 = e5m2x2_to_f16x2((uint16_t)(gv[e / 2] >> (16 * (e & 1))));
+                const float2 gf = __half22float2(*reinterpret_cast<const __half2*>(&g2));
+                float2 of;
+                if constexpr (kBF16)
+                    of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[e]));
+                else
+                    of = __half22float2(*reinterpret_cast<const __half2*>(&ov[e]));
+                acc = fmaf(gf.x, of.x, acc);
+                acc = fmaf(gf.y, of.y, acc);
+            }
+        }
+#pragma unroll
+        for (int s = kLanes / 2; s > 0; s >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, s);
+        if (row[k] < rows && c == 0) {
+            const int hq = (int)(row[k] % Hq);
+            const int64_t bi = row[k] / Hq;
+            const int i = (int)(bi % Sq);
+            const int b = (int)(bi / Sq);
+            delta[((int64_t)b * Hq + hq) * Sq + i] = acc;
+        }
     }
 }
 
