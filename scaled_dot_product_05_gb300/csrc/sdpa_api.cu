@@ -74,11 +74,11 @@ struct DeviceState {
 };
 DeviceState g_dev[kMaxDevices];
 
-template <int D, int KIND, bool kPacked = false>
+template <int D, int KIND, bool kPacked = false, int QT = 2>
 cudaError_t set_attrs()
 {
-    return cudaFuncSetAttribute(sdpa::sdpa_fwd_kernel<D, KIND, kPacked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                sdpa::Layout<D, KIND>::kSmemBytes);
+    return cudaFuncSetAttribute(sdpa::sdpa_fwd_kernel<D, KIND, kPacked, QT>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, sdpa::Layout<D, KIND, QT>::kSmemBytes);
 }
 
 template <int D, int KIND>
@@ -120,7 +120,9 @@ sdpa_status_t device_ready(int* dev_out, int* sm_count)
             st.err = e3;
             return;
         }
-        cudaError_t es[] = {set_attrs<32, sdpa::kBF16>(),        set_attrs<32, sdpa::kFP16>(),
+        cudaError_t es[] = {set_attrs<32, sdpa::kBF16, false, 1>(), set_attrs<32, sdpa::kFP16, false, 1>(),
+                            set_attrs<64, sdpa::kBF16, false, 1>(), set_attrs<64, sdpa::kFP16, false, 1>(),
+                            set_attrs<32, sdpa::kBF16>(),        set_attrs<32, sdpa::kFP16>(),
                             set_attrs<64, sdpa::kBF16>(),        set_attrs<64, sdpa::kFP16>(),
                             set_attrs<64, sdpa::kE4M3>(),        set_attrs<128, sdpa::kBF16>(),
                             set_attrs<128, sdpa::kFP16>(),       set_attrs<128, sdpa::kE4M3>(),
@@ -261,8 +263,9 @@ sdpa_status_t check_common(const Args& a, int in_elem_bytes, int out_elem_bytes)
     // D = 32 only for 16-bit elements: E4M3 rows would be 32 bytes
     if (s.D != 64 && s.D != 128 && !(s.D == 32 && in_elem_bytes == 2))
         return SDPA_ERR_HEAD_DIM;
-    // the B * Hq * ceil(Sq / 256) work units are counted in int
-    const int64_t n_pairs = (static_cast<int64_t>(s.Sq) + sdpa::kUnitRows - 1) / sdpa::kUnitRows;
+    // the B * Hq * ceil(Sq / 128) work units (at most: units of one Q tile)
+    // are counted in int
+    const int64_t n_pairs = (static_cast<int64_t>(s.Sq) + sdpa::kBlockM - 1) / sdpa::kBlockM;
     if (static_cast<int64_t>(s.B) * s.Hq * n_pairs > INT32_MAX)
         return SDPA_ERR_BAD_SHAPE;
     if (!strides_ok(a.q, in_elem_bytes) || !strides_ok(a.k, in_elem_bytes) || !strides_ok(a.v, in_elem_bytes) ||
@@ -367,14 +370,17 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
     return true;
 }
 
-template <int D, int KIND, bool kPacked = false>
+template <int D, int KIND, bool kPacked = false, int QT = 2>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                    const sdpa::Params& p, int sm_count, cudaStream_t stream)
 {
-    // persistent: one CTA per SM (each takes all 512 TMEM columns)
-    const unsigned grid = static_cast<unsigned>(p.n_units < sm_count ? p.n_units : sm_count);
-    sdpa::sdpa_fwd_kernel<D, KIND, kPacked>
-        <<<grid, sdpa::kThreads, sdpa::Layout<D, KIND>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
+    // persistent: one CTA per SM (all 512 TMEM columns), or two per SM with
+    // one Q tile each (256 columns each)
+    using R = sdpa::Roles<QT>;
+    const long long slots = static_cast<long long>(sm_count) * R::kCtasPerSm;
+    const unsigned grid = static_cast<unsigned>(p.n_units < slots ? p.n_units : slots);
+    sdpa::sdpa_fwd_kernel<D, KIND, kPacked, QT>
+        <<<grid, R::kThreads, sdpa::Layout<D, KIND, QT>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
     cudaError_t e = cudaGetLastError();
     if constexpr (kPacked) {
         if (e == cudaSuccess && p.part_o) {
@@ -388,7 +394,24 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
     return e;
 }
 
-sdpa::Params make_params(const Args& a, double score_scale, float out_scale, int causal)
+// Q tiles per CTA of the standard forward pass.  One (two CTAs per SM, each
+// loading its own K / V) for 16-bit kinds at D <= 64 when units of two Q
+// tiles would fill at most two rounds of the SMs: there the finer units
+// balance the causal work and one CTA's unit boundaries overlap the other's
+// key tiles.  Else two (one CTA per SM, both tiles reading each K / V tile).
+// Measured at D = 64, one against two: causal B=4 H=16 S=1024 (1.7 rounds)
+// +6 %, the B=4 T=128 latency row +5 %; causal B=16 S=1024 (6.7 rounds) -6 %,
+// causal S=2048..8192 -3 to -6 %, non-causal S=2048..16384 within 1 %.
+int fwd_q_tiles(bool fp8, const Shape& s, int sm_count)
+{
+    if (fp8 || s.D > 64)
+        return 2;
+    const long long units2 =
+        static_cast<long long>(s.B) * s.Hq * ((s.Sq + sdpa::kUnitRows - 1) / sdpa::kUnitRows);
+    return units2 <= 2LL * sm_count ? 1 : 2;
+}
+
+sdpa::Params make_params(const Args& a, double score_scale, float out_scale, int causal, int unit_rows)
 {
     const Shape& s = a.s;
     sdpa::Params p{};
@@ -403,7 +426,7 @@ sdpa::Params make_params(const Args& a, double score_scale, float out_scale, int
     p.Sq = s.Sq;
     p.Skv = s.Skv;
     p.group = s.Hq / s.Hkv;
-    p.n_pairs = (s.Sq + sdpa::kUnitRows - 1) / sdpa::kUnitRows;
+    p.n_pairs = (s.Sq + unit_rows - 1) / unit_rows;
     p.n_units = s.B * s.Hq * p.n_pairs;
     p.n_ktiles = (s.Skv + sdpa::kBlockN - 1) / sdpa::kBlockN;
     p.causal = causal ? 1 : 0;
@@ -413,13 +436,22 @@ sdpa::Params make_params(const Args& a, double score_scale, float out_scale, int
 }
 
 template <int KIND>
-cudaError_t launch_kind(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_kind(int D, int qt, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& to, const sdpa::Params& p, int sm_count, cudaStream_t stream)
 {
-    if (D == 32) {
-        if constexpr (KIND != sdpa::kE4M3)
+    // qt from fwd_q_tiles(), which also sized the units in p: one Q tile per
+    // CTA only for 16-bit kinds at D <= 64
+    if constexpr (KIND != sdpa::kE4M3) {
+        if (qt == 1 && D == 32)
+            return launch<32, KIND, false, 1>(tq, tk, tv, to, p, sm_count, stream);
+        if (qt == 1 && D == 64)
+            return launch<64, KIND, false, 1>(tq, tk, tv, to, p, sm_count, stream);
+        if (qt == 1)
+            return cudaErrorInvalidValue;       // never chosen at D = 128
+        if (D == 32)
             return launch<32, KIND>(tq, tk, tv, to, p, sm_count, stream);
-        return cudaErrorInvalidValue;           // rejected by check_common
+    } else if (D == 32 || qt != 2) {
+        return cudaErrorInvalidValue;           // rejected by check_common / never chosen
     }
     return D == 64 ? launch<64, KIND>(tq, tk, tv, to, p, sm_count, stream)
                    : launch<128, KIND>(tq, tk, tv, to, p, sm_count, stream);
@@ -469,11 +501,12 @@ sdpa_status_t run(const Args& a, float scale, const float* descales, int causal,
         !make_map(&to, a.O, dt_o, 2, s.D, s.Hq, s.Sq, s.B, a.o, 1, 32))
         return cuda_fail(cudaErrorInvalidValue);
 
-    const sdpa::Params p = make_params(a, score_scale, out_scale, causal);
+    const int qt = fwd_q_tiles(fp8, s, sm_count);
+    const sdpa::Params p = make_params(a, score_scale, out_scale, causal, qt * sdpa::kBlockM);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = fp8 ? launch_kind<sdpa::kE4M3>(s.D, tq, tk, tv, to, p, sm_count, cs)
-                        : dtype == SDPA_DTYPE_BF16 ? launch_kind<sdpa::kBF16>(s.D, tq, tk, tv, to, p, sm_count, cs)
-                                                   : launch_kind<sdpa::kFP16>(s.D, tq, tk, tv, to, p, sm_count, cs);
+    const cudaError_t e = fp8 ? launch_kind<sdpa::kE4M3>(s.D, qt, tq, tk, tv, to, p, sm_count, cs)
+                        : dtype == SDPA_DTYPE_BF16 ? launch_kind<sdpa::kBF16>(s.D, qt, tq, tk, tv, to, p, sm_count, cs)
+                                                   : launch_kind<sdpa::kFP16>(s.D, qt, tq, tk, tv, to, p, sm_count, cs);
     if (e != cudaSuccess)
         return cuda_fail(e);
     return SDPA_OK;
@@ -560,7 +593,7 @@ sdpa_status_t run_decode(const Args& a, float scale, sdpa_dtype_t dtype, void* w
         !make_map(&tv, a.V, dt, 2, s.D, s.Hkv, s.Skv, s.B, a.v))
         return cuda_fail(cudaErrorInvalidValue);
 
-    sdpa::Params p = make_params(a, scale, 1.f, 0);
+    sdpa::Params p = make_params(a, scale, 1.f, 0, sdpa::kUnitRows);
     p.n_pairs = d.n_pairs;
     p.n_units = static_cast<int>(d.units);
     p.tiles_per_split = d.tiles_per_split;

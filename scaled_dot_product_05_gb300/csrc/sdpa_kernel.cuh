@@ -16,6 +16,10 @@
 //   warp 8       TMA producer: Q tiles, then K_j / V_j into shared-memory rings
 //   warps 9, 10  tcgen05 issue of O_t += P_t V_j for Q tile 0 / 1
 //   warp 11      tcgen05 issue of every S_t = Q_t K_j^T
+// A second instance (QT = 1, 16-bit kinds at D <= 64, small problems) runs
+// two CTAs per SM with units of one Q tile: 8 warps (softmax 0..3, producer
+// 4, P V issue 5, S issue 7), half the TMEM columns and ~100 KB of shared
+// memory each; see Roles below.
 // Both Q tiles take turns in one TMEM S region.  P_t never overwrites S: the
 // 16-bit P_t has its own TMEM columns, the E4M3 P_t sits in shared memory
 // (and the tensor core sums its rows, P_t times a tile of ones).  So S_t(j+1)
@@ -48,17 +52,34 @@ namespace sdpa {
 
 constexpr int kBlockM = 128;         // query rows per Q tile (= TMEM lanes)
 constexpr int kBlockN = 128;         // keys per K/V tile
-constexpr int kUnitRows = 2 * kBlockM;
-constexpr int kThreads = 384;        // 12 warps
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;          // P V issue for Q tile 0; warp 10 for Q tile 1
-constexpr int kSMmaWarp = 11;        // S issue
-// Register split: launched at 168 per thread (384 x 168 = 64512); the
-// producer warpgroup (warps 8..11) drops to 104 and the two softmax warpgroups
-// rise to 192: 128 x 104 + 256 x 192 = 62464 <= 64512.
-constexpr uint32_t kRegsProducer = 104;
-constexpr uint32_t kRegsSoftmax = 192;
-static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * 168, "register split exceeds the launch budget");
+// Warp roles for QT Q tiles per CTA.  QT = 2 (the standard pass, one CTA
+// per SM): warps 0..7 are two softmax warpgroups, warp 8 the TMA producer,
+// warps 9 / 10 the P V issuers of Q tile 0 / 1, warp 11 the S issuer; both
+// Q tiles read every K / V tile the CTA loads.  QT = 1 (16-bit kinds at
+// D <= 64, two CTAs per SM): warps 0..3 softmax, 4 producer, 5 P V issuer,
+// 7 S issuer (warp 6 idles); the two CTAs of an SM run independent units of
+// one Q tile each, so a unit's epilogue overlaps the other CTA's key tiles.
+template <int QT>
+struct Roles {
+    static_assert(QT == 1 || QT == 2, "Q tiles per CTA");
+    static constexpr int kUnitRows = QT * kBlockM;
+    static constexpr int kThreads = 128 * QT + 128;
+    static constexpr int kProducerWarp = 4 * QT;
+    static constexpr int kMmaWarp = 4 * QT + 1;      // P V issue for Q tile 0 (+ 1: Q tile 1)
+    static constexpr int kSMmaWarp = 4 * QT + 3;     // S issue
+    static constexpr int kCtasPerSm = 3 - QT;
+    // Register split: launched at 168 per thread (QT = 2: 384 x 168 = 64512)
+    // or 128 (QT = 1: two CTAs of 256 x 128); the producer warpgroup drops to
+    // 104 / 64 and the softmax warpgroups rise to 192.
+    static constexpr uint32_t kLaunchRegs = (QT == 2) ? 168u : 128u;
+    static constexpr uint32_t kRegsProducer = (QT == 2) ? 104u : 64u;
+    static constexpr uint32_t kRegsSoftmax = 192;
+    static_assert(128 * kRegsProducer + 128 * QT * kRegsSoftmax <= kThreads * kLaunchRegs,
+                  "register split exceeds the launch budget");
+    static_assert(kThreads * kLaunchRegs * kCtasPerSm <= 65536, "register file");
+};
+// the standard pass's unit (also the packed decode pass's)
+constexpr int kUnitRows = Roles<2>::kUnitRows;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per barrier wait
 constexpr float kRescaleThreshold = 8.0f;          // log2 units: rescale O when m grows by > 2^8
 // E4M3 P: rescale when m grows by > 2^3 and store P * 56, so that
@@ -121,9 +142,10 @@ enum Kind : int { kBF16 = 0, kFP16 = 1, kE4M3 = 2 };
 // A Q / K / V tile is 128 rows of D elements; TMA writes it as column blocks
 // ("chunks") of kSwz bytes per row with the matching hardware swizzle
 // (128-byte, or 64-byte when a row holds only 64 bytes).
-template <int D, int KIND>
+template <int D, int KIND, int QT = 2>
 struct Layout {
     static_assert(D == 32 || D == 64 || D == 128, "head dimension");
+    static_assert(QT == 2 || (KIND != kE4M3 && D <= 64), "one Q tile per CTA: 16-bit kinds, D <= 64");
     static_assert(D != 32 || KIND != kE4M3, "E4M3 needs rows of at least 64 bytes");
     static constexpr int kEsize = (KIND == kE4M3) ? 1 : 2;
     static constexpr int kRowBytes = D * kEsize;
@@ -137,11 +159,14 @@ struct Layout {
     static constexpr int kKeysPerStep = 32 / kEsize;                   // P V MMAs: 16 (16-bit) or 32 (8-bit) keys
     static constexpr int kPVSteps = kBlockN / kKeysPerStep;
     // 16-bit D = 128 keeps 2 K stages, E4M3 D = 128 3 V stages, so that the
-    // output staging below fits
-    static constexpr int kStagesK = (kTileBytes >= 32768) ? 2 : 4;
-    static constexpr int kStagesV = (kTileBytes >= 32768) ? 2 : (KIND == kE4M3 && D == 128) ? 3 : 4;
-    static constexpr int kOffQ = 0;                                    // Q tile 0, Q tile 1
-    static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+    // output staging below fits; one Q tile per CTA keeps 2 + 2 stages of
+    // 16 KB tiles, so that two CTAs fit on an SM
+    static constexpr int kStagesK = (kTileBytes >= 32768 || (QT == 1 && kTileBytes >= 16384)) ? 2 : 4;
+    static constexpr int kStagesV = (kTileBytes >= 32768 || (QT == 1 && kTileBytes >= 16384)) ? 2
+                                    : (KIND == kE4M3 && D == 128)                                 ? 3
+                                                                                                  : 4;
+    static constexpr int kOffQ = 0;                                    // Q tile 0 (, Q tile 1)
+    static constexpr int kOffK = kOffQ + QT * kTileBytes;
     static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
     // E4M3: P_t lives in shared memory (128 rows x 128 keys, one byte each,
     // 128-byte swizzled rows), one tile per Q tile; 16-bit P stays in TMEM.
@@ -160,25 +185,29 @@ struct Layout {
     static constexpr int kOWarpBytes = 32 * kOSwz;
     static constexpr int kOffO = (KIND == kE4M3) ? kOffOnes + kOnesBytes : kOffP;
     static_assert(kOffO % 1024 == 0, "output staging must sit on a swizzle-atom boundary");
-    static constexpr int kOffBar = kOffO + 8 * kOWarpBytes;
+    static constexpr int kOffBar = kOffO + 4 * QT * kOWarpBytes;
     static constexpr int kBarBytes = 1024;
     static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;     // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    // TMEM columns (512).  O_t takes the last 2 x D columns.  Both Q tiles
-    // take turns in one S region (columns 0..127), except for 16-bit kinds at
-    // D = 64, where each has its own (128 t).  (E4M3 keeps the shared region
+    static_assert(QT == 2 || 2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
+    // TMEM columns (512, or 256 with one Q tile per CTA).  O_t takes the last
+    // QT x D columns.  Both Q tiles take turns in one S region (columns
+    // 0..127), except for 16-bit kinds at D = 64, where each has its own (128 t).  (E4M3 keeps the shared region
     // at D = 64 too: it staggers the two softmax warpgroups, whose exp phases
     // otherwise collide on the MUFU.)  After the S columns: 16-bit P_t (64
     // columns each, two values per column) or, for E4M3 (P in shared memory),
     // the row sums l_t (16 columns each, all equal).
-    static constexpr bool kSharedS = (D > 64) || (KIND == kE4M3);
+    static constexpr bool kSharedS = (D > 64) || (KIND == kE4M3) || (QT == 1);
+    static constexpr uint32_t kTmemCols = (QT == 2) ? 512u : 256u;
     static constexpr uint32_t kAfterS = kSharedS ? 128u : 256u;
     __host__ __device__ static constexpr uint32_t tmem_s(int t) { return kSharedS ? 0u : 128u * t; }
     __host__ __device__ static constexpr uint32_t tmem_p(int t) { return kAfterS + 64u * t; }  // 16-bit kinds
     __host__ __device__ static constexpr uint32_t tmem_l(int t) { return kAfterS + 16u * t; }  // E4M3
-    __host__ __device__ static constexpr uint32_t tmem_o(int t) { return 512u - 2u * D + (uint32_t)D * t; }
-    static_assert(kAfterS + 128u <= 512u - 2u * D, "TMEM columns overlap");
-    static constexpr uint32_t kTmemCols = 512;
+    __host__ __device__ static constexpr uint32_t tmem_o(int t)
+    {
+        return kTmemCols - (uint32_t)(QT * D) + (uint32_t)D * t;
+    }
+    static_assert(kAfterS + 64u * QT <= kTmemCols - (uint32_t)(QT * D), "TMEM columns overlap");
 };
 
 template <int NK, int NV>
@@ -259,7 +288,7 @@ struct Unit {
 // head h of the group), so a K/V tile serves every head of the group at once;
 // the key range may be split over several units.  Non-causal only.
 // Unit u -> (KV head, batch, packed-row pair, split), KV head fastest.
-template <bool kPacked>
+template <bool kPacked, int QT = 2>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u)
 {
     Unit w;
@@ -288,6 +317,14 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u)
     w.b = bh / p.Hq;
     w.hq = bh % p.Hq;
     w.hkv = w.hq / p.group;
+    if constexpr (QT == 1) {
+        // one Q tile (w.pair is its index): causal rows of tile i see keys
+        // below 128 (i + 1)
+        w.n_kv[0] = p.causal ? min(p.n_ktiles, w.pair + 1) : p.n_ktiles;
+        w.n_kv[1] = 0;
+        w.n = w.n_kv[0];
+        return w;
+    }
     if (p.causal) {
         w.n_kv[0] = min(p.n_ktiles, 2 * w.pair + 1);
         w.n_kv[1] = min(p.n_ktiles, 2 * w.pair + 2);
@@ -343,11 +380,11 @@ __device__ __forceinline__ uint64_t desc_join(uint32_t hi, uint32_t lo)
 // kKeysPerStep keys is kKeysPerStep rows of kSwz bytes, the next chunk of D
 // columns kChunkBytes further (LBO).  The E4M3 P tile and the ones tile have
 // 128-byte rows: one 128-byte swizzle span, 8-row groups 1024 bytes apart.
-template <int D, int KIND, bool kPacked, int NK, int NV>
+template <int D, int KIND, bool kPacked, int NK, int NV, int QT>
 __device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
                                             uint32_t tmem, uint32_t sQ, uint32_t sK)
 {
-    using L = Layout<D, KIND>;
+    using L = Layout<D, KIND, QT>;
     constexpr uint32_t kFmt = (KIND == kBF16) ? 1u : 0u;          // bf16 / f16 / E4M3
     constexpr uint32_t idesc_s = idesc_make(kFmt, kBlockM, kBlockN, false);
     constexpr uint32_t kTileUnits = L::kTileBytes >> 4;
@@ -364,7 +401,7 @@ __device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* b
             break;
         if (u < 0)
             continue;
-        const Unit w = decode_unit<kPacked>(p, u);
+        const Unit w = decode_unit<kPacked, QT>(p, u);
         const int n = w.n;
         for (int j = 0; ok && j < n; ++j) {
             ok = wait_bar(smem_u32(&bars->k_full[ck % NK]), (ck / NK) & 1, abort, kErrWaitMma + 3);
@@ -417,13 +454,13 @@ __device__ __forceinline__ void mma_issue_s(const Params& p, Barriers<NK, NV>* b
 // O_t (+)= P_t V_j for Q tile t, kKeysPerStep keys per MMA.  16-bit P_t is
 // read from its TMEM columns (8 columns per step of 16 keys).  E4M3 P_t
 // (K-major, keys contiguous) comes from shared memory, and l_t (+)= P_t x
-// ones.  Both P V threads release every V slot of the unit (barrier count 2),
-// tile 0 also the causal key tile it does not visit.
-template <int D, int KIND, bool kPacked, int NK, int NV>
+// ones.  Every P V thread (QT of them) releases every V slot of the unit
+// (barrier count QT), tile 0 also the causal key tile it does not visit.
+template <int D, int KIND, bool kPacked, int NK, int NV, int QT>
 __device__ __forceinline__ void mma_issue_pv(const Params& p, Barriers<NK, NV>* bars, volatile int* abort,
                                              uint32_t tmem, uint32_t sV, uint32_t sP, uint32_t sOnes, int t)
 {
-    using L = Layout<D, KIND>;
+    using L = Layout<D, KIND, QT>;
     constexpr bool kFP8 = (KIND == kE4M3);
     constexpr uint32_t kFmt = (KIND == kBF16) ? 1u : 0u;
     constexpr uint32_t idesc_o = idesc_make(kFmt, kBlockM, D, true);
@@ -447,7 +484,7 @@ __device__ __forceinline__ void mma_issue_pv(const Params& p, Barriers<NK, NV>* 
             break;
         if (u < 0)
             continue;
-        const Unit w = decode_unit<kPacked>(p, u);
+        const Unit w = decode_unit<kPacked, QT>(p, u);
         const int n = w.n;
         const int nt = w.n_kv[t];
         for (int j = 0; ok && j < n; ++j, ++cv) {
@@ -507,12 +544,13 @@ __device__ __forceinline__ void mma_issue_pv(const Params& p, Barriers<NK, NV>* 
 
 // tm_o: O as [B][Sq][Hq][D] with the caller's strides, box {kOSwz bytes of a
 // row, 1 head, 32 rows, 1 batch}; unused in packed mode.
-template <int D, int KIND, bool kPacked>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int KIND, bool kPacked, int QT = 2>
+__global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
 sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, const Params p)
 {
-    using L = Layout<D, KIND>;
+    using L = Layout<D, KIND, QT>;
+    using R = Roles<QT>;
     constexpr bool kFP8 = (KIND == kE4M3);
     constexpr bool kOutBF16 = (KIND != kFP16);         // E4M3 inputs give a bf16 output
     constexpr int NK = L::kStagesK;
@@ -547,7 +585,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         for (int s = 0; s < NV; ++s) {
             mbar_init(smem_u32(&bars->v_full[s]), 1);
-            mbar_init(smem_u32(&bars->v_empty[s]), 2);          // released by both P V issuers
+            mbar_init(smem_u32(&bars->v_empty[s]), QT);         // released by every P V issuer
         }
         mbar_init(smem_u32(&bars->s_free[0]), 128);
         mbar_init(smem_u32(&bars->s_free[1]), 128);
@@ -557,20 +595,20 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bars->s_issued[0] = bars->s_issued[1] = 0;
         fence_mbar_init();
     }
-    if (warp == kProducerWarp && lane == 0) {
+    if (warp == R::kProducerWarp && lane == 0) {
         tma_prefetch_map(&tm_q);
         tma_prefetch_map(&tm_k);
         tma_prefetch_map(&tm_v);
         if constexpr (!kPacked)
             tma_prefetch_map(&tm_o);
     }
-    if (warp == kMmaWarp) {
+    if (warp == R::kMmaWarp) {
         tmem_alloc(smem_u32(&bars->tmem_base), L::kTmemCols);
         tmem_relinquish();
     }
     if constexpr (kFP8) {
         uint32_t* ones = reinterpret_cast<uint32_t*>(smem + L::kOffOnes);
-        for (int i = threadIdx.x; i < L::kOnesBytes / 4; i += kThreads)
+        for (int i = threadIdx.x; i < L::kOnesBytes / 4; i += R::kThreads)
             ones[i] = 0x38383838u;
         fence_proxy_async_smem();                      // read by tcgen05.mma
     }
@@ -579,9 +617,9 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp >= 8) {
-      regs_release<kRegsProducer>();
-      if (warp == kProducerWarp) {
+    if (warp >= R::kProducerWarp) {
+      regs_release<R::kRegsProducer>();
+      if (warp == R::kProducerWarp) {
         // =========================== TMA producer ===========================
         if (lane == 0) {
             uint32_t nk = 0, nv = 0;             // K / V tiles issued (ring position)
@@ -593,7 +631,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive_expect_tx(smem_u32(&bars->q_full[t]), L::kTileBytes);
                 // packed: the tensor map's box is {chunk, G heads, 128 / G positions},
                 // so one copy brings rows s * G + h of the KV head's query heads
-                const int r0 = w.pair * kUnitRows + t * kBlockM;
+                const int r0 = w.pair * R::kUnitRows + t * kBlockM;
                 const int h = kPacked ? w.hkv * p.group : w.hq;
                 const int s0 = kPacked ? r0 / p.group : r0;
                 for (int c = 0; c < L::kChunks; ++c)
@@ -636,7 +674,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     break;
                 if (u < 0)
                     continue;
-                const Unit w = decode_unit<kPacked>(p, u);
+                const Unit w = decode_unit<kPacked, QT>(p, u);
                 const int n = w.n;
                 ok = load_q(w, 0) && load_k(w, 0) && (w.n_kv[1] == 0 || load_q(w, 1)) && load_v(w, 0);
                 for (int j = 1; ok && j < n; ++j)
@@ -656,19 +694,19 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     drain_wait(smem_u32(&bars->v_full[i % NV]), (i / NV) & 1);
             }
         }
-      } else if (warp == kSMmaWarp) {
+      } else if (warp == R::kSMmaWarp) {
         // ============================= S issuer =============================
         if (lane == 0)
-            mma_issue_s<D, KIND, kPacked, NK, NV>(p, bars, abort, tmem, sQ, sK);
-      } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+            mma_issue_s<D, KIND, kPacked, NK, NV, QT>(p, bars, abort, tmem, sQ, sK);
+      } else if (warp >= R::kMmaWarp && warp < R::kMmaWarp + QT) {
         // =========================== P V issuers ============================
         if (lane == 0) {
-            mma_issue_pv<D, KIND, kPacked, NK, NV>(p, bars, abort, tmem, sV, sP, smem_u32(smem + L::kOffOnes),
-                                                  warp - kMmaWarp);
+            mma_issue_pv<D, KIND, kPacked, NK, NV, QT>(p, bars, abort, tmem, sV, sP, smem_u32(smem + L::kOffOnes),
+                                                  warp - R::kMmaWarp);
         }
       }
     } else {
-        regs_acquire<kRegsSoftmax>();
+        regs_acquire<R::kRegsSoftmax>();
         // ========================= softmax warpgroups =======================
         const int t = warp >> 2;                           // Q tile of this warpgroup
         const int quarter = warp & 3;                      // TMEM lanes 32*quarter ..
@@ -702,13 +740,13 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 break;
             if (u < 0)
                 continue;
-            const Unit w = decode_unit<kPacked>(p, u);
+            const Unit w = decode_unit<kPacked, QT>(p, u);
             const int n = w.n_kv[t];
             if (n == 0)
                 continue;                                  // this Q tile has no rows in the unit
             // this thread's row: query position q_idx of head hq (packed:
             // row r of the KV head's stacked heads, r = q_idx * G + head)
-            const int r_all = w.pair * kUnitRows + t * kBlockM + row;
+            const int r_all = w.pair * R::kUnitRows + t * kBlockM + row;
             const int q_idx = kPacked ? r_all / p.group : r_all;
             const int hq = kPacked ? w.hkv * p.group + r_all % p.group : w.hq;
             int limit = p.Skv - 1;                         // last key this row sees
@@ -897,7 +935,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 // 64-byte rows), then one TMA store per pass.  Rows past Sq
                 // are clipped by the store.
                 const uint32_t stage = sO + (uint32_t)warp * L::kOWarpBytes;
-                const int q_warp = w.pair * kUnitRows + t * kBlockM + quarter * 32;   // first row of the warp
+                const int q_warp = w.pair * R::kUnitRows + t * kBlockM + quarter * 32;   // first row of the warp
                 constexpr int kUnits = L::kOSwz / 16;
                 const uint32_t swz = (L::kOSwz == 128) ? (uint32_t)(lane & 7) : (uint32_t)((lane >> 1) & 3);
 #pragma unroll
@@ -932,7 +970,7 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == R::kMmaWarp) {
         __syncwarp();
         tc_fence_after_sync();
         tmem_dealloc(tmem, L::kTmemCols);

@@ -155,6 +155,19 @@ def test_batch_sweep_t256_full(B):
     assert_close(to_np(o), ref, "bf16", f"batch {B}")
 
 
+# At D <= 64 the 16-bit pass runs one Q tile per CTA (two CTAs per SM) when
+# units of two Q tiles would fill at most two rounds of the SMs (304 units on
+# 152 SMs), else two Q tiles per CTA.  The shapes above are all below that
+# line; these (B=8, Hq=16, S=1000: 512 two-tile units, ragged last tile, GQA
+# 4:1) are above it, so both layouts meet the oracle at D = 32 and 64 (the
+# small shapes run both 16-bit kinds through the one-tile layout).
+@pytest.mark.parametrize("D", [32, 64])
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+def test_two_tile_ctas_at_small_head_dims_sampled(D, causal):
+    x = make_qkv(40 + D, 8, 16, 4, 1000, 1000, D, "bf16")
+    sampled_check(x, causal, 1500, 50 + D)
+
+
 def test_causal_gqa_4096_sampled():
     x = make_qkv(2, 2, 32, 8, 4096, 4096, 128, "bf16")
     sampled_check(x, True, 3000, 2)
