@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 #include <utility>
 
 #include <cuda.h>
@@ -325,15 +326,38 @@ struct MapKey {
     int dt, elem_bytes, D, H, S, B, box_h, box_s;
 };
 
+// Tensor maps of earlier calls, per host thread.  Encoding one costs ~2 us of
+// driver time, more than the rest of a small call; a call whose buffers,
+// shapes and strides were seen before (a training or serving loop reuses its
+// activation buffers, one model has a few maps per attention layer) finds its
+// maps here.  Open addressing over kSlots entries, kProbes probes from the
+// key's hash, replacement taking turns within the probe window.  The table
+// (~0.8 MB) is allocated on a thread's first call.
 struct MapCache {
-    static constexpr int kSize = 32;
-    MapKey key[kSize];
-    CUtensorMap map[kSize];
-    bool used[kSize] = {};
-    int next = 0;
+    static constexpr uint32_t kSlots = 4096;     // a power of two
+    static constexpr uint32_t kProbes = 8;
+    struct Entry {
+        CUtensorMap map;
+        MapKey key;
+        bool used;
+    };
+    std::vector<Entry> e = std::vector<Entry>(kSlots);
+    uint32_t turn = 0;
 };
 
 thread_local MapCache t_maps;
+
+// FNV-1a over the key's bytes (its padding is zeroed), folded
+uint64_t map_key_hash(const MapKey& k)
+{
+    const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < sizeof k; ++i) {
+        h ^= b[i];
+        h *= 1099511628211ull;
+    }
+    return h ^ (h >> 32);
+}
 
 // box_h x box_s (heads x rows) per copy: 1 x 128, or G x 128 / G for packed
 // query tiles.
@@ -355,18 +379,27 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
     k.box_h = box_h;
     k.box_s = box_s;
     MapCache& c = t_maps;
-    for (int i = 0; i < MapCache::kSize; ++i)
-        if (c.used[i] && std::memcmp(&c.key[i], &k, sizeof k) == 0) {
-            *map = c.map[i];
+    const uint32_t h = static_cast<uint32_t>(map_key_hash(k));
+    uint32_t free_slot = MapCache::kSlots;
+    for (uint32_t i = 0; i < MapCache::kProbes; ++i) {
+        MapCache::Entry& x = c.e[(h + i) & (MapCache::kSlots - 1)];
+        if (!x.used) {
+            if (free_slot == MapCache::kSlots)
+                free_slot = (h + i) & (MapCache::kSlots - 1);
+        } else if (std::memcmp(&x.key, &k, sizeof k) == 0) {
+            *map = x.map;
             return true;
         }
+    }
     if (!encode_map(map, base, dt, elem_bytes, D, H, S, B, st, box_h, box_s))
         return false;
-    const int slot = c.next;
-    c.next = (c.next + 1) % MapCache::kSize;
-    std::memcpy(&c.key[slot], &k, sizeof k);
-    c.map[slot] = *map;
-    c.used[slot] = true;
+    const uint32_t slot = free_slot != MapCache::kSlots
+                              ? free_slot
+                              : (h + c.turn++ % MapCache::kProbes) & (MapCache::kSlots - 1);
+    MapCache::Entry& x = c.e[slot];
+    std::memcpy(&x.key, &k, sizeof k);
+    x.map = *map;
+    x.used = true;
     return true;
 }
 

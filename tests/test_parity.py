@@ -97,6 +97,34 @@ def test_deterministic():
     assert torch.equal(a, b)
 
 
+def test_tensor_map_cache_many_buffer_sets():
+    # 1100 sets of Q, K, V, O buffers (4400 tensor maps, more than the
+    # library's per-thread cache holds), cycled twice: the second pass mixes
+    # cache hits with evictions and re-encodes, and must reproduce the first
+    # pass bit for bit; a few sets are also checked against the oracle
+    from scaled_dot_product_05_gb300 import sdpa_fwd
+    dev = torch.device("cuda:0")
+    x = make_qkv(77, 1, 2, 1, 130, 130, 64, "bf16")
+    base = [t.to(dev) for t in (x.q, x.k, x.v)]
+    n = 1100
+    # distinct buffers and outputs at the inputs' own scale: Q rolled along
+    # the sequence, K and V copied
+    sets = [(torch.roll(base[0], i % 130, dims=1), base[1].clone(), base[2].clone()) for i in range(n)]
+    outs = [torch.empty_like(base[0]) for _ in range(n)]
+    for i in range(n):
+        sdpa_fwd(*sets[i], outs[i], causal=(i % 2 == 1))
+    first = [o.clone() for o in outs]
+    for i in range(n):
+        outs[i].fill_(0)
+        sdpa_fwd(*sets[i], outs[i], causal=(i % 2 == 1))
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(first, outs))
+    for i in (0, 1, 777):
+        q, k, v = (t.cpu() for t in sets[i])
+        ref = oracle.sdpa_reference(q, k, v, causal=(i % 2 == 1), dtype="bf16")
+        assert_close(to_np(outs[i]), ref, "bf16", f"set {i}")
+
+
 def test_output_guard_bands_untouched():
     from scaled_dot_product_05_gb300 import sdpa_fwd
     x = make_qkv(9, 1, 2, 2, 200, 200, 128, "bf16")
