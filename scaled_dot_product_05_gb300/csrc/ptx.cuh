@@ -126,6 +126,20 @@ __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* map, uint32
 
 // 4-D tiled store shared -> global (TMA); elements outside the tensor are not
 // written.  Tracked by the issuing thread's bulk async-group.
+// Programmatic dependent launch (a launch with the programmatic stream
+// serialization attribute may start before the previous kernel in its stream
+// has finished): wait until every grid this launch depends on has completed
+// and its memory is visible -- returns at once without such a dependency --
+// and let the next such launch in the stream be scheduled.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2, int c3)
 {
     asm volatile(

@@ -412,9 +412,22 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
     using R = sdpa::Roles<QT>;
     const long long slots = static_cast<long long>(sm_count) * R::kCtasPerSm;
     const unsigned grid = static_cast<unsigned>(p.n_units < slots ? p.n_units : slots);
-    sdpa::sdpa_fwd_kernel<D, KIND, kPacked, QT>
-        <<<grid, R::kThreads, sdpa::Layout<D, KIND, QT>::kSmemBytes, stream>>>(tq, tk, tv, to, p);
-    cudaError_t e = cudaGetLastError();
+    // programmatic dependent launch: the CTAs may start their prologue while
+    // the previous kernel in the stream finishes; the kernel waits for it
+    // (griddepcontrol.wait) before touching global memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(R::kThreads);
+    cfg.dynamicSmemBytes = sdpa::Layout<D, KIND, QT>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, sdpa::sdpa_fwd_kernel<D, KIND, kPacked, QT>, tq, tk, tv, to, p);
+    if (e == cudaSuccess)
+        e = cudaGetLastError();
     if constexpr (kPacked) {
         if (e == cudaSuccess && p.part_o) {
             // merge the key-range splits: one warp per output row

@@ -616,6 +616,13 @@ sdpa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
+    // Everything above touches only this CTA's shared memory, TMEM and the
+    // kernel's parameters, so with a programmatic dependent launch it runs
+    // while the previous kernel in the stream finishes.  Global memory (inputs
+    // that kernel may still be writing, outputs it may still be reading) only
+    // after it has completed; then the next launch may be scheduled.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp >= R::kProducerWarp) {
       regs_release<R::kRegsProducer>();

@@ -161,6 +161,23 @@ def test_lse_closed_form_zero_query():
     assert np.abs(got - want[None, None, :]).max() <= 1e-5
 
 
+@pytest.mark.parametrize("D", [32, 64])
+def test_two_tile_ctas_small_head_dim_bhsd_lse_sampled(D):
+    # D <= 64 above the one-tile threshold (B=8, Hq=16, S=1000: 512 units of
+    # two Q tiles), BHSD in and out, LSE; the small shapes above cover the
+    # one-tile layout with every layout
+    B, Hq, Hkv, S = 8, 16, 4, 1000
+    x = make_qkv(350 + D, B, Hq, Hkv, S, S, D, "bf16")
+    o, lse = run_ex(x, True, "bhsd", "bhsd")
+    rows = sample_rows(3 + D, B, S, Hq, 600)
+    ref, ref_lse = oracle.sdpa_reference(x.q, x.k, x.v, causal=True, dtype="bf16", rows=rows, return_lse=True)
+    flat = to_np(o.contiguous()).reshape(-1, D)
+    assert_close(flat[rows], ref, "bf16", f"two-tile d{D} bhsd")
+    l = lse.cpu().double().numpy()
+    got = np.array([l[r // (Hq * S), r % Hq, (r // Hq) % S] for r in rows])
+    assert np.abs(got - ref_lse).max() <= LSE_TOL["bf16"]
+
+
 def test_causal_gqa_4096_bhsd_lse_sampled():
     # the headline workload with BHSD layouts and the LSE, sampled rows
     B, Hq, Hkv, S, D = 2, 32, 8, 4096, 128
