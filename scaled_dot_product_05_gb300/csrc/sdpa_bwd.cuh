@@ -231,6 +231,10 @@ sdpa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
+    // programmatic dependent launch: global memory only after the previous
+    // kernel in the stream (the Delta pass) has completed
+    grid_dependency_wait();
+    grid_launch_dependents();
     // (head, query tile) of iteration it: head-major with ascending query
     // tiles; for causal passes with 8 or more query heads per KV head, query
     // tiles from the last down with the heads innermost, so that the CTAs of

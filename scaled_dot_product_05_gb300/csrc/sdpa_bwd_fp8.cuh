@@ -218,6 +218,10 @@ sdpa_bwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
+    // programmatic dependent launch: global memory only after the previous
+    // kernel in the stream (the Delta pass) has completed
+    grid_dependency_wait();
+    grid_launch_dependents();
     // (head, query tile) of iteration it: head-major with ascending query
     // tiles; for causal passes with 8 or more query heads per KV head, query
     // tiles from the last down with the heads innermost, so that the CTAs of
@@ -601,6 +605,8 @@ template <int D, bool kBF16>
 __global__ void __launch_bounds__(256) bwd8_delta_kernel(const void* O, const void* dO8, float* delta,
                                                          uint16_t* dq_acc, unsigned int* amax, int B, int Hq, int Sq)
 {
+    grid_dependency_wait();                       // launched with programmatic serialization
+    grid_launch_dependents();
     constexpr int kLanes = D / 16;
     constexpr int kGroups = 256 / kLanes;
     const int64_t rows = (int64_t)B * Sq * Hq;
@@ -657,6 +663,8 @@ __global__ void __launch_bounds__(256) bwd8_delta_kernel(const void* O, const vo
 // dQ (bf16, [B][Sq][Hq][D]) = factor * the bf16 accumulator, 8 elements a thread.
 __global__ void __launch_bounds__(256) bwd8_dq_convert_kernel(const uint16_t* acc, void* dQ, int64_t n, float factor)
 {
+    grid_dependency_wait();                       // launched with programmatic serialization
+    grid_launch_dependents();
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (i >= n)
         return;

@@ -34,6 +34,8 @@ template <int D, bool kBF16>
 __global__ void __launch_bounds__(kDeltaThreads) bwd_delta_kernel(const void* O, const void* dO, float* delta,
                                                                   float* dq_acc, int B, int Hq, int Sq)
 {
+    grid_dependency_wait();                       // launched with programmatic serialization
+    grid_launch_dependents();
     constexpr int kLanes = D / 8;
     constexpr int kGroups = kDeltaThreads / kLanes;
     const int64_t rows = (int64_t)B * Sq * Hq;
@@ -89,6 +91,8 @@ __global__ void __launch_bounds__(kDeltaThreads) bwd_delta_kernel(const void* O,
 template <bool kBF16>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* acc, void* dQ, int64_t n)
 {
+    grid_dependency_wait();                       // launched with programmatic serialization
+    grid_launch_dependents();
     const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
     if (i >= n)
         return;
