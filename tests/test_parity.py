@@ -50,6 +50,8 @@ SMALL = [
     (1, 2, 1, 1, 500, 64),
     (1, 2, 2, 500, 1, 128),
     (1, 6, 3, 640, 640, 128),
+    (1, 6, 2, 300, 300, 128),      # 3 query heads per KV head: causal units of two tiles of one head
+    (2, 8, 2, 1100, 1100, 128),    # causal, Sq > 1024: two tiles of one head even for an even group
     (2, 4, 2, 300, 300, 32),
     (1, 8, 8, 129, 520, 32),
 ]
