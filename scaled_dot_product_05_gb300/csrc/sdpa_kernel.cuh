@@ -192,11 +192,12 @@ struct Layout {
     static_assert(QT == 2 || 2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
     // TMEM columns (512, or 256 with one Q tile per CTA).  O_t takes the last
     // QT x D columns.  Both Q tiles take turns in one S region (columns
-    // 0..127), except for 16-bit kinds at D = 64, where each has its own (128 t).  (E4M3 keeps the shared region
-    // at D = 64 too: it staggers the two softmax warpgroups, whose exp phases
-    // otherwise collide on the MUFU.)  After the S columns: 16-bit P_t (64
-    // columns each, two values per column) or, for E4M3 (P in shared memory),
-    // the row sums l_t (16 columns each, all equal).
+    // 0..127), except for 16-bit kinds at D = 64 with two Q tiles, where each
+    // has its own (128 t).  (E4M3 keeps the shared region at D = 64 too: it
+    // measured faster there, the shared region staggering the two softmax
+    // warpgroups.)  After the S columns: 16-bit P_t (64 columns each, two
+    // values per column) or, for E4M3 (P in shared memory), the row sums l_t
+    // (16 columns each, all equal).
     static constexpr bool kSharedS = (D > 64) || (KIND == kE4M3) || (QT == 1);
     static constexpr uint32_t kTmemCols = (QT == 2) ? 512u : 256u;
     static constexpr uint32_t kAfterS = kSharedS ? 128u : 256u;
