@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from sdpa_inputs import make_qkv, sample_rows
-from tests.parity import assert_close, to_np
+from tests.parity import GROWING, assert_close, growing_inputs, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -196,6 +196,20 @@ def test_batch_sweep_t256_full(B):
 def test_two_tile_ctas_at_small_head_dims_sampled(D, causal):
     x = make_qkv(40 + D, 8, 16, 4, 1000, 1000, D, "bf16")
     sampled_check(x, causal, 1500, 50 + D)
+
+
+# The running max grows by at least 11 (exp2 units; checked on these inputs)
+# from each full key tile to the next, so every row takes the lazy rescale (O
+# and l times 2^(m_old - m_new), taken when the max grows by more than 8) on
+# every tile after its first: query component 0 is 4 and key j's component 0
+# is 32 j / 128.  N(0,1) inputs seldom take that path.
+@pytest.mark.parametrize("shape,dtype", GROWING, ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else v)
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_growing_max_rescales_every_tile(shape, dtype, causal):
+    x = growing_inputs(shape, dtype)
+    o = run_gpu(x, causal)
+    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=causal, dtype=dtype)
+    assert_close(to_np(o), ref, dtype, f"growing max {shape} causal={causal}")
 
 
 def test_causal_gqa_4096_sampled():
