@@ -38,7 +38,8 @@ class QKV:
         return sum(t.numel() * t.element_size() for t in (self.q, self.k, self.v))
 
 
-def _quantise_e4m3(x: torch.Tensor):
+def quantise_e4m3(x: torch.Tensor):
+    """x -> (E4M3 codes of x * 448 / amax|x|, descale amax / 448)."""
     amax = float(x.abs().max())
     s = torch.tensor(E4M3_MAX / amax, dtype=torch.float32)
     x8 = (x * s).to(torch.float8_e4m3fn)
@@ -58,7 +59,7 @@ def make_qkv(seed: int, B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int,
     if dtype == "fp16":
         return QKV(q.to(torch.float16), k.to(torch.float16), v.to(torch.float16), dtype, (1.0, 1.0, 1.0))
     if dtype == "e4m3":
-        (q8, dq), (k8, dk), (v8, dv) = _quantise_e4m3(q), _quantise_e4m3(k), _quantise_e4m3(v)
+        (q8, dq), (k8, dk), (v8, dv) = quantise_e4m3(q), quantise_e4m3(k), quantise_e4m3(v)
         return QKV(q8, k8, v8, dtype, (dq, dk, dv))
     raise ValueError(f"unknown dtype {dtype!r}")
 

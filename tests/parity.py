@@ -9,7 +9,7 @@ the cuDNN fused backend")."""
 import numpy as np
 import torch
 
-from sdpa_inputs import make_qkv
+from sdpa_inputs import QKV, make_qkv, quantise_e4m3
 
 TOL = {"bf16": (1e-2, 4e-3), "fp16": (1e-2, 4e-3), "e4m3": (6e-2, None)}
 
@@ -41,18 +41,23 @@ def assert_close(got, ref, dtype, what=""):
 # tests/test_rescale_inputs.py); query component 0 is 4, key j's component 0
 # is 32 j / 128.
 GROWING = [((1, 4, 2, 1024, 1024, 128), "bf16"), ((2, 4, 4, 700, 700, 64), "bf16"),
-           ((1, 2, 1, 640, 900, 128), "fp16"), ((1, 8, 2, 300, 1000, 32), "bf16")]
+           ((1, 2, 1, 640, 900, 128), "fp16"), ((1, 8, 2, 300, 1000, 32), "bf16"),
+           ((1, 4, 2, 768, 768, 128), "e4m3"), ((2, 4, 4, 500, 500, 64), "e4m3")]
 
 
 def growing_inputs(shape, dtype):
     B, Hq, Hkv, Sq, Skv, D = shape
-    x = make_qkv(900 + D + Sq, B, Hq, Hkv, Sq, Skv, D, dtype)
+    x = make_qkv(900 + D + Sq, B, Hq, Hkv, Sq, Skv, D, "bf16" if dtype == "e4m3" else dtype)
     q, k = x.q.float(), x.k.float()
     q[..., 0] = 4.0
     k[..., 0] = (32.0 * torch.arange(Skv, dtype=torch.float32) / 128.0).view(1, Skv, 1)
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
     # V halved: with the weights on a few keys |O| approaches max |V| (~4.5),
     # where one 16-bit rounding unit of O is already near the absolute bound;
     # a rescale mistake would still err by the order of |O|
-    x.q, x.k, x.v = q.to(tdt), k.to(tdt), (x.v.float() * 0.5).to(tdt)
+    v = x.v.float() * 0.5
+    if dtype == "e4m3":
+        (q8, dq), (k8, dk), (v8, dv) = quantise_e4m3(q), quantise_e4m3(k), quantise_e4m3(v)
+        return QKV(q8, k8, v8, "e4m3", (dq, dk, dv))
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    x.q, x.k, x.v = q.to(tdt), k.to(tdt), v.to(tdt)
     return x

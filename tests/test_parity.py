@@ -207,8 +207,12 @@ def test_two_tile_ctas_at_small_head_dims_sampled(D, causal):
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 def test_growing_max_rescales_every_tile(shape, dtype, causal):
     x = growing_inputs(shape, dtype)
-    o = run_gpu(x, causal)
-    ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=causal, dtype=dtype)
+    if dtype == "e4m3":
+        o = run_gpu_fp8(x, causal)
+        ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=causal, dtype="e4m3", descales=x.descales)
+    else:
+        o = run_gpu(x, causal)
+        ref = oracle.sdpa_reference(x.q, x.k, x.v, causal=causal, dtype=dtype)
     assert_close(to_np(o), ref, dtype, f"growing max {shape} causal={causal}")
 
 
