@@ -95,3 +95,62 @@ def test_backward_chain_of_short_calls():
         return res
     a, b = run(False), run(True)
     assert all(torch.equal(x, y) for ra, rb in zip(a, b) for x, y in zip(ra, rb))
+
+
+def test_cuda_graph_of_chained_calls():
+    # the same chains captured in a CUDA graph (programmatic launches become
+    # programmatic dependency edges) and replayed: identical to eager calls
+    from scaled_dot_product_05_gb300 import sdpa_bwd, sdpa_fwd, sdpa_fwd_ex
+    q, k, v = _qkv(800, 2, 4, 4, 256, 64)
+    n = 8
+    # eager chain, each call reading the previous output as its Q
+    eager = [q]
+    for i in range(n):
+        eager.append(sdpa_fwd(eager[-1], k, v, causal=(i % 2 == 0)))
+    torch.cuda.synchronize()
+    # captured chain into preallocated outputs
+    outs = [torch.empty_like(q) for _ in range(n)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        src = q
+        for i in range(n):              # warm-up on the capture stream
+            sdpa_fwd(src, k, v, outs[i], causal=(i % 2 == 0))
+            src = outs[i]
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for o in outs:
+        o.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        src = q
+        for i in range(n):
+            sdpa_fwd(src, k, v, outs[i], causal=(i % 2 == 0))
+            src = outs[i]
+    g.replay()
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(eager[1:], outs))
+
+    # a short backward call (its three kernels chained) in a graph
+    B = 1
+    qb, kb, vb = q[:B].contiguous(), k[:B].contiguous(), v[:B].contiguous()
+    o = torch.empty_like(qb)
+    lse = torch.empty((B, 4, 256), dtype=torch.float32, device=DEV)
+    sdpa_fwd_ex(qb, kb, vb, o, lse, causal=True)
+    do = (torch.randn_like(qb) * 0.1).contiguous()
+    from scaled_dot_product_05_gb300 import bwd_workspace_bytes
+    ws = torch.empty(bwd_workspace_bytes(B, 4, 256, 64), dtype=torch.uint8, device=DEV)
+    ref = sdpa_bwd(qb, kb, vb, o, do, lse, causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    grads = tuple(torch.empty_like(t) for t in ref)
+    with torch.cuda.stream(side):
+        sdpa_bwd(qb, kb, vb, o, do, lse, *grads, causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    for t in grads:
+        t.zero_()
+    gb = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gb):
+        sdpa_bwd(qb, kb, vb, o, do, lse, *grads, causal=True, workspace=ws)
+    gb.replay()
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(ref, grads))
